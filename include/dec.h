@@ -1,0 +1,199 @@
+/*
+ * dec.h -- C ABI of the GB300 batch-1 decode step (persistent megakernel).
+ *
+ * What the library computes is one autoregressive decode step of a pre-norm
+ * transformer at batch 1, or a verify window of up to 4 tokens:
+ *   x <- E[token] (or a given hidden vector)
+ *   per layer: a = RMSNorm(x); [q;k;v] = W_qkv a; RoPE(q, k, pos); cache[pos] <- bf16(k, v);
+ *              o = GQA attention over cache[0..pos]; x += W_o o;
+ *              b = RMSNorm(x); x += SwiGLU(b) (dense) or shared + top-k routed experts (MoE)
+ *   logits = W_lm RMSNorm(x); token = argmax(logits)
+ * Sources: batch-1 decode as matrix-vector weight streaming (Kog, "3k tokens/s
+ * per request", section "what limits decode speed on GPUs"); one resident
+ * kernel chaining the ops instead of one launch per op (Muse Spark Open
+ * megakernel article, sections "the baseline nobody benchmarked" and "where
+ * the kernel boundary sits"); MoE top-8 of 512 + 1 shared expert in MXFP4, a
+ * dynamic FP8 LM head and a k-token verify window (Ling-3.0-flash on DGX Spark,
+ * sections "model and baseline configuration", "optimisation 1/2/3").
+ *
+ * Conventions for every call:
+ *   - No exception crosses the ABI: every call returns a dec_status; the text of
+ *     the last error of the calling thread is dec_last_error().
+ *   - Device memory is owned by the caller (weights, KV cache, workspace). The
+ *     library keeps pointers, never frees them and allocates no device memory.
+ *   - Work is ordered on the CUDA stream given to dec_init. A call synchronises
+ *     the host only where it copies a result to a host pointer.
+ *   - A device-side failure (a dependency wait that ran out of time) is sticky:
+ *     later calls return DEC_ERR_STATE until dec_reset.
+ *   - Matrices are logical [rows = out_features][cols = in_features], row-major.
+ */
+#ifndef DEC_H
+#define DEC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DEC_OK = 0,
+  DEC_ERR_INVALID_ARG = 1, /* null pointer, misaligned pointer, bad enum */
+  DEC_ERR_SHAPE = 2,       /* dimension not supported or inconsistent with the config */
+  DEC_ERR_DTYPE = 3,       /* tensor dtype tag does not match the config */
+  DEC_ERR_STATE = 4,       /* call out of order, missing weights, or sticky device error */
+  DEC_ERR_CUDA = 5,        /* a CUDA runtime call failed */
+  DEC_ERR_TIMEOUT = 6,     /* a device dependency wait ran out of time (sticky) */
+  DEC_ERR_CAPACITY = 7,    /* pos + window exceeds the KV capacity, or token >= vocab */
+} dec_status;
+
+typedef enum {
+  DEC_BF16 = 0,            /* bfloat16 values, 2 B per weight */
+  DEC_FP8_E4M3_ROWSCALE = 1, /* e4m3fn codes, 1 B per weight, plus one fp32 scale per row */
+  DEC_MXFP4 = 2,           /* e2m1 codes (2 per byte, even element low nibble) plus one
+                              E8M0 scale byte per 32 consecutive weights of a row */
+} dec_dtype;
+
+typedef enum {
+  DEC_MODE_PERSISTENT = 0, /* one cooperative launch per step; ops chained by device counters */
+  DEC_MODE_PER_OP = 1,     /* the same kernel launched once per op (launch-per-op comparison) */
+  DEC_MODE_PER_OP_GRAPH = 2, /* the per-op launches of one step replayed as a CUDA graph */
+} dec_mode;
+
+typedef struct {
+  int n_layers;      /* decoder layers (0: LM head only) */
+  int hidden;        /* H, multiple of 64 */
+  int n_q, n_kv;     /* attention heads (n_q = 0: no attention block); n_q % n_kv == 0 */
+  int head_dim;      /* must be 128 */
+  int ffn;           /* dense SwiGLU width F (0: no dense FFN), multiple of 8 */
+  int n_experts;     /* routed experts E (0: no MoE FFN) */
+  int top_k;         /* routed experts per token, 1..8 */
+  int moe_inter;     /* expert intermediate I, multiple of 32 */
+  int n_shared;      /* shared experts (weight 1), 0..1 */
+  int vocab;         /* V (0: no LM head) */
+  int kv_capacity;   /* positions the KV cache holds */
+  int max_verify;    /* largest window (tokens per call), 1..4 */
+  int embedding;     /* 1: a step starts from E[token]; 0: from a given hidden vector */
+  int final_norm;    /* 1: RMSNorm before the LM head */
+  float rms_eps;     /* RMSNorm epsilon */
+  float rope_base;   /* RoPE base (rotate-half pairing (i, i + d/2)) */
+  dec_dtype lm_head_dtype; /* DEC_BF16 or DEC_FP8_E4M3_ROWSCALE */
+  dec_dtype expert_dtype;  /* DEC_MXFP4 */
+  dec_mode mode;
+  uint64_t spin_timeout_ns; /* limit of every device wait (0: 2 s) */
+  int num_ctas;      /* persistent CTAs (0: one per SM) */
+} dec_config;
+
+typedef struct dec_ctx dec_ctx;
+
+/* Kinds of weight tensors passed to dec_load_weights. Packed layouts are the
+   ones dec_pack / dec_pack_pair write. */
+typedef enum {
+  DEC_T_EMBED = 0,       /* [V][H] bf16 (embedding = 1 only) */
+  DEC_T_ATTN_NORM = 1,   /* [H] bf16 gain */
+  DEC_T_WQKV = 2,        /* [(n_q + 2 n_kv) d][H] bf16: q heads, then k heads, then v heads */
+  DEC_T_WO = 3,          /* [H][n_q d] bf16 */
+  DEC_T_FFN_NORM = 4,    /* [H] bf16 gain */
+  DEC_T_WGATEUP = 5,     /* [2F][H] bf16, rows interleaved gate_0, up_0, gate_1, ... (dec_pack_pair) */
+  DEC_T_WDOWN = 6,       /* [H][F] bf16 */
+  DEC_T_WROUTER = 7,     /* [E][H] bf16 */
+  DEC_T_EXPERT_GATEUP = 8, /* all experts of a layer: E + n_shared matrices [2I][H] MXFP4 pair-
+                              interleaved; values contiguous per expert, scales contiguous per
+                              expert; expert e >= E is shared expert e - E */
+  DEC_T_EXPERT_DOWN = 9, /* all experts of a layer: E + n_shared matrices [H][I] MXFP4 */
+  DEC_T_FINAL_NORM = 10, /* [H] bf16 gain */
+  DEC_T_LM_HEAD = 11,    /* [V][H] bf16, or FP8 codes + fp32 row scales */
+} dec_tensor_kind;
+
+typedef struct {
+  dec_tensor_kind kind;
+  int layer;             /* layer index, 0 for head tensors */
+  dec_dtype dtype;       /* tag checked against the config */
+  int rows, cols;        /* logical shape of one matrix (per expert for expert tensors) */
+  const void* values;    /* device pointer, 16-byte aligned */
+  const void* scales;    /* device pointer of the scale plane (FP8, MXFP4), else NULL */
+} dec_tensor;
+
+/* Bytes of device workspace dec_init needs for this config (0 on an invalid config). */
+size_t dec_workspace_bytes(const dec_config* cfg);
+
+/* Validate cfg, bind the CUDA stream (cudaStream_t, NULL = legacy default) and the
+   caller's workspace (dec_workspace_bytes long, 256-byte aligned, any contents: it is
+   cleared here), and create a context on the current device. */
+dec_status dec_init(const dec_config* cfg, void* cuda_stream, void* workspace_dev, dec_ctx** out);
+
+/* Register packed weight tensors (device pointers, caller-owned and kept alive until
+   dec_free). Tags and shapes are checked against the config; may be called repeatedly. */
+dec_status dec_load_weights(dec_ctx* ctx, const dec_tensor* tensors, int n);
+
+/* Register the KV cache: k_dev and v_dev are bf16 [n_layers][n_kv][kv_capacity][head_dim].
+   Positions below the step's pos must hold the cached (already rotated) keys and values. */
+dec_status dec_set_kv_cache(dec_ctx* ctx, void* k_dev, void* v_dev);
+
+/* One decode step of `token` at position `pos` (embedding configs), or of the given hidden
+   vector hidden_dev (bf16 [H], device; non-embedding configs, token ignored).
+   Writes the new key/value at pos. logits_dev (nullable, fp32 [V], device) receives the
+   logits; argmax_host (nullable) receives the greedy token and makes the call wait. */
+dec_status dec_step(dec_ctx* ctx, int32_t token, const void* hidden_dev, int32_t pos,
+                    float* logits_dev, int32_t* argmax_host);
+
+/* n greedy steps chained on the device: step i feeds the argmax of step i-1 (the first one
+   feeds `token`) at position pos + i. No host synchronisation between steps.
+   tokens_dev (nullable, int32 [n], device) receives the n generated tokens. */
+dec_status dec_generate(dec_ctx* ctx, int32_t token, int32_t pos, int n, int32_t* tokens_dev);
+
+/* Verify window: tokens_host[i] (i < k <= max_verify) is fed at pos + i in one pass, each
+   seeing positions 0..pos+i. logits_dev (nullable, fp32 [k][V]); argmax_host (nullable,
+   [k]); n_accepted (nullable): the longest j with tokens[i+1] == argmax[i] for all i < j,
+   plus one (the model's own next token). Non-embedding configs pass hidden_dev (bf16 [k][H])
+   and tokens_host may be NULL. Keys/values of all k positions are written. */
+dec_status dec_verify(dec_ctx* ctx, const int32_t* tokens_host, const void* hidden_dev, int k,
+                      int32_t pos, float* logits_dev, int32_t* argmax_host, int32_t* n_accepted);
+
+/* Device pointer of the residual stream after every block of the last call: fp32
+   [2 n_layers + 1][max_verify][H] (entry 0 is the input, then after attention and after
+   the FFN of each layer), and of the qkv projections fp32 [n_layers][max_verify][qkv rows].
+   For inspection and tests; valid until the next call on the stream. */
+dec_status dec_debug_buffers(dec_ctx* ctx, const float** hidden, const float** qkv,
+                             const int32_t** routing);
+
+/* Clear a sticky device error: resets counters and the status word (stream-ordered). */
+dec_status dec_reset(dec_ctx* ctx);
+
+/* Wait for the context's stream; returns a sticky device error if one was raised. */
+dec_status dec_sync(dec_ctx* ctx);
+
+/* Number of kernel launches the last dec_step / dec_verify issued (1 in persistent mode). */
+int dec_last_launch_count(dec_ctx* ctx);
+
+/* Text of the last error raised on the calling thread ("" if none). */
+const char* dec_last_error(void);
+
+void dec_free(dec_ctx* ctx);
+
+/* ---------------------------------------------------------------- packer (host)
+   Quantise / lay out one logical bf16 matrix [rows][cols] (host memory) into the packed
+   layout the kernels stream. Sizes: dec_packed_bytes. Rules:
+   - DEC_BF16: values copied as is.
+   - DEC_FP8_E4M3_ROWSCALE (Ling-3.0-flash DGX Spark article, "optimisation 2: online FP8 LM
+     head"): per row s = amax / 448 in IEEE fp32 (zero row: s = 1), code =
+     e4m3fn(round-to-nearest-even of w / s, fp32 division), saturated to +-448.
+   - DEC_MXFP4 (OCP MX v1.0): per 32 weights along a row, E8M0 e = floor(log2 amax) - 2 + 127
+     clamped to [0, 254] (all-zero block: e = 0); code = e2m1(round-to-nearest-even of
+     w / 2^(e-127)) saturated to +-6, sign bit = sign of w; values plane [rows][cols/2]
+     then scales plane [rows][cols/32].
+   out_scales may be NULL for DEC_BF16. */
+dec_status dec_packed_bytes(dec_dtype dtype, int rows, int cols, size_t* values_bytes,
+                            size_t* scales_bytes);
+dec_status dec_pack(dec_dtype dtype, const uint16_t* bf16_host, int rows, int cols,
+                    void* out_values, void* out_scales);
+/* Interleave two [rows][cols] matrices row by row (a_0, b_0, a_1, b_1, ...) into a packed
+   [2 rows][cols] matrix: the gate/up layout of DEC_T_WGATEUP and DEC_T_EXPERT_GATEUP. */
+dec_status dec_pack_pair(dec_dtype dtype, const uint16_t* a_host, const uint16_t* b_host, int rows,
+                         int cols, void* out_values, void* out_scales);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DEC_H */

@@ -1,0 +1,854 @@
+// Host side of the C ABI declared in include/dec.h: config validation, workspace layout,
+// the step's op list, launch modes (persistent / per op / per-op CUDA graph) and the
+// sticky device status.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/dec.h"
+#include "dec_internal.h"
+
+using namespace decimpl;
+
+extern "C" cudaError_t dec_launch_megakernel(const KParams* kp, int cooperative, cudaStream_t stream);
+extern "C" size_t dec_megakernel_smem_bytes(int nslot, int act_bytes);
+extern "C" int dec_megakernel_common_bytes(void);
+
+namespace {
+
+thread_local std::string g_last_error;
+
+dec_status fail(dec_status code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+#define CUDA_TRY(expr)                                                                     \
+  do {                                                                                     \
+    cudaError_t e_ = (expr);                                                               \
+    if (e_ != cudaSuccess) return fail(DEC_ERR_CUDA, "%s: %s", #expr, cudaGetErrorString(e_)); \
+  } while (0)
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct LayerW {
+  const void* attn_norm = nullptr;
+  const void* wqkv = nullptr;
+  const void* wo = nullptr;
+  const void* ffn_norm = nullptr;
+  const void* wgateup = nullptr;
+  const void* wdown = nullptr;
+  const void* wrouter = nullptr;
+  const void* egu_v = nullptr;
+  const void* egu_s = nullptr;
+  const void* edn_v = nullptr;
+  const void* edn_s = nullptr;
+};
+
+struct Layout {  // byte offsets into the workspace
+  size_t state, status, ctr, tickets, ops, hs, qkv, attn_out, hbuf, rlogits, route, eh, part, logits, am_val, am_idx,
+      am_out, total;
+  int n_ops, n_tickets, n_ctas, ns_max, nslot, act_bytes;
+};
+
+bool validate(const dec_config* c, std::string& why) {
+  auto bad = [&](const char* m) { why = m; return false; };
+  if (!c) return bad("null config");
+  if (c->n_layers < 0 || c->hidden <= 0 || c->hidden % 64) return bad("hidden must be a positive multiple of 64");
+  if (c->max_verify < 1 || c->max_verify > kMmax) return bad("max_verify must be 1..4");
+  const bool attn = c->n_q > 0;
+  if (c->n_layers > 0 && !attn && c->ffn == 0 && c->n_experts == 0) return bad("layers without blocks");
+  if (attn) {
+    if (c->head_dim != kHeadDim) return bad("head_dim must be 128");
+    if (c->n_kv <= 0 || c->n_q % c->n_kv) return bad("n_q must be a multiple of n_kv");
+    if (c->n_q / c->n_kv > 8) return bad("at most 8 query heads per kv head");
+    if (c->kv_capacity < 1) return bad("kv_capacity must be positive");
+  }
+  if (c->ffn < 0 || c->ffn % 8) return bad("ffn must be a multiple of 8");
+  if (c->ffn && c->n_experts) return bad("a layer is dense or MoE, not both");
+  if (c->n_experts) {
+    if (c->top_k < 1 || c->top_k > 8 || c->top_k > c->n_experts) return bad("top_k must be 1..min(8, E)");
+    if (c->moe_inter <= 0 || c->moe_inter % 32) return bad("moe_inter must be a positive multiple of 32");
+    if (c->n_shared < 0 || c->n_shared > 1) return bad("n_shared must be 0 or 1");
+    if (c->expert_dtype != DEC_MXFP4) return bad("expert_dtype must be DEC_MXFP4");
+    if ((2LL * c->moe_inter * (c->hidden / 32)) % 16 || (1LL * c->hidden * (c->moe_inter / 32)) % 16)
+      return bad("MXFP4 scale planes of one expert must be multiples of 16 bytes");
+  }
+  if (c->vocab < 0) return bad("vocab must be >= 0");
+  if (c->vocab && c->lm_head_dtype != DEC_BF16 && c->lm_head_dtype != DEC_FP8_E4M3_ROWSCALE)
+    return bad("lm_head_dtype must be DEC_BF16 or DEC_FP8_E4M3_ROWSCALE");
+  if (c->embedding && c->vocab <= 0) return bad("embedding needs a vocabulary");
+  if (c->mode < DEC_MODE_PERSISTENT || c->mode > DEC_MODE_PER_OP_GRAPH) return bad("bad mode");
+  if (c->num_ctas < 0) return bad("num_ctas must be >= 0");
+  if (!std::isfinite(c->rms_eps) || c->rms_eps < 0) return bad("rms_eps must be >= 0");
+  return true;
+}
+
+int ctas_for(const dec_config* c) {
+  if (c->num_ctas > 0) return c->num_ctas;
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+int count_ops(const dec_config* c) {
+  int n = 0;
+  for (int l = 0; l < c->n_layers; ++l) {
+    if (c->n_q) n += 3;
+    if (c->ffn) n += 2;
+    if (c->n_experts) n += 3 + (c->n_shared ? 1 : 0);
+  }
+  if (c->vocab) n += 1;
+  return n;
+}
+
+int pow2_floor(int v) {
+  int p = 1;
+  while (p * 2 <= v) p *= 2;
+  return p;
+}
+
+int gcd(int a, int b) { return b ? gcd(b, a % b) : a; }
+
+// Tile geometry of a [N][K] matrix of dtype wt: threads per row group and rows per tile.
+void tile_geometry(int wt, int K, int pair, int& tpr, int& rpt, int& unit) {
+  const int cw = wt == W_BF16 ? 8 : (wt == W_FP8 ? 16 : 32);
+  const int nv = K / cw;
+  tpr = std::min(kConsumerThreads, std::max(32, pow2_floor(nv)));
+  const int rows_max = (kConsumerThreads / tpr) * kRmax;
+  const int rb = wt == W_BF16 ? 2 * K : (wt == W_FP8 ? K : K / 2);
+  const int sb = wt == W_MXFP4 ? K / 32 : 0;
+  unit = pair ? 2 : 1;
+  if (wt == W_MXFP4) {
+    const int us = 16 / gcd(16, sb);
+    unit = unit * us / gcd(unit, us);
+  }
+  int r = std::min(rows_max, kSlotBytes / (rb + sb));
+  while (r > 0 && (((size_t)r * rb + 15) / 16 * 16 + (size_t)r * sb > (size_t)kSlotBytes)) --r;
+  r = r / unit * unit;
+  rpt = r;
+}
+
+bool compute_layout(const dec_config* c, Layout& L, std::string& why) {
+  const int C = ctas_for(c);
+  if (C <= 0) {
+    why = "no CUDA device to size the grid (set num_ctas)";
+    return false;
+  }
+  const int M = c->max_verify, H = c->hidden, nl = c->n_layers;
+  const int G = c->n_q ? c->n_q / c->n_kv : 1;
+  const int qkv_rows = c->n_q ? (c->n_q + 2 * c->n_kv) * kHeadDim : 0;
+  L.n_ctas = C;
+  L.n_ops = count_ops(c);
+  L.ns_max = c->n_q ? std::max(1, C / c->n_kv) : 1;
+  L.n_tickets = (c->n_q ? nl * c->n_kv : 0) + (c->n_experts ? nl : 0) + 1 + 1;
+
+  // shared-memory scratch ("act") the largest op needs
+  size_t act = (size_t)M * H * 4;
+  act = std::max(act, (size_t)2 * kConsumerThreads * 4);
+  if (c->n_q) {
+    const size_t MG = (size_t)M * G;
+    act = std::max(act, (size_t)M * c->n_q * kHeadDim * 4);
+    act = std::max(act, (MG * 128 + MG * 64 + 96 + 2 * kMmax * 256 / 4 + 16 * 128 + MG * L.ns_max) * 4);
+  }
+  if (c->ffn) act = std::max(act, (size_t)M * c->ffn * 4);
+  if (c->n_experts) {
+    act = std::max(act, (size_t)M * c->n_experts * 4);
+    const int rows_cta = (H + C - 1) / C + 16;
+    act = std::max(act, ((size_t)kMmax * c->moe_inter + (size_t)rows_cta * M) * 4);
+  }
+  act = align_up(act, 16);
+  const int common = dec_megakernel_common_bytes();
+  const long long room = (long long)kSmemLimit - (long long)act - common;
+  const int nslot = (int)std::min<long long>(kMaxSlots, room / kSlotBytes);
+  if (nslot < 2) {
+    why = "shapes need more shared memory than a CTA has";
+    return false;
+  }
+  L.nslot = nslot;
+  L.act_bytes = (int)act;
+
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align_up(o + bytes, 256);
+    return at;
+  };
+  L.state = take(sizeof(StepState));
+  L.status = take(sizeof(Status));
+  L.ctr = take((size_t)std::max(1, L.n_ops) * 4);
+  L.tickets = take((size_t)L.n_tickets * 4);
+  L.ops = take((size_t)std::max(1, L.n_ops) * sizeof(OpDesc));
+  L.hs = take((size_t)(2 * nl + 1) * M * H * 4);
+  L.qkv = take((size_t)nl * M * qkv_rows * 4);
+  L.attn_out = take((size_t)nl * M * c->n_q * kHeadDim * 4);
+  L.hbuf = take((size_t)nl * M * c->ffn * 4);
+  L.rlogits = take((size_t)nl * M * c->n_experts * 4);
+  L.route = take((size_t)(c->n_experts ? nl : 0) * sizeof(RouteBlock));
+  L.eh = take((size_t)(c->n_experts ? nl : 0) * kMaxRouteSlots * M * c->moe_inter * 4);
+  L.part = take((size_t)(c->n_q ? c->n_kv : 0) * L.ns_max * M * G * 130 * 4);
+  L.logits = take((size_t)M * c->vocab * 4);
+  L.am_val = take((size_t)C * kMmax * 4);
+  L.am_idx = take((size_t)C * kMmax * 4);
+  L.am_out = take((size_t)kMmax * 4);
+  L.total = o;
+  return true;
+}
+
+}  // namespace
+
+struct dec_ctx {
+  dec_config cfg;
+  cudaStream_t stream;
+  uint8_t* ws;
+  Layout lay;
+  std::vector<LayerW> layers;
+  const void* embed = nullptr;
+  const void* final_norm = nullptr;
+  const void* lm_v = nullptr;
+  const void* lm_s = nullptr;
+  uint16_t* kc = nullptr;
+  uint16_t* vc = nullptr;
+  bool ops_dirty = true;
+  std::vector<OpDesc> ops;
+  KParams kp;
+  bool sticky = false;
+  dec_status sticky_code = DEC_OK;
+  cudaGraphExec_t graph = nullptr;
+  int last_launches = 0;
+};
+
+namespace {
+
+template <class T>
+T* wsp(dec_ctx* c, size_t off) {
+  return reinterpret_cast<T*>(c->ws + off);
+}
+
+dec_status check_weights(dec_ctx* c) {
+  const dec_config& g = c->cfg;
+  for (int l = 0; l < g.n_layers; ++l) {
+    const LayerW& w = c->layers[l];
+    if (g.n_q && (!w.attn_norm || !w.wqkv || !w.wo)) return fail(DEC_ERR_STATE, "layer %d: attention weights missing", l);
+    if ((g.ffn || g.n_experts) && !w.ffn_norm) return fail(DEC_ERR_STATE, "layer %d: ffn_norm missing", l);
+    if (g.ffn && (!w.wgateup || !w.wdown)) return fail(DEC_ERR_STATE, "layer %d: dense FFN weights missing", l);
+    if (g.n_experts && (!w.wrouter || !w.egu_v || !w.egu_s || !w.edn_v || !w.edn_s))
+      return fail(DEC_ERR_STATE, "layer %d: MoE weights missing", l);
+  }
+  if (g.embedding && !c->embed) return fail(DEC_ERR_STATE, "embedding missing");
+  if (g.vocab && (!c->lm_v || (g.final_norm && !c->final_norm))) return fail(DEC_ERR_STATE, "LM head missing");
+  if (g.vocab && g.lm_head_dtype == DEC_FP8_E4M3_ROWSCALE && !c->lm_s) return fail(DEC_ERR_STATE, "LM head scales missing");
+  if (g.n_q && (!c->kc || !c->vc)) return fail(DEC_ERR_STATE, "KV cache not set");
+  return DEC_OK;
+}
+
+void build_ops(dec_ctx* c) {
+  const dec_config& g = c->cfg;
+  const Layout& L = c->lay;
+  const int C = L.n_ctas, M = g.max_verify, H = g.hidden;
+  const int qkv_rows = g.n_q ? (g.n_q + 2 * g.n_kv) * kHeadDim : 0;
+  float* hs = wsp<float>(c, L.hs);
+  std::vector<OpDesc>& ops = c->ops;
+  ops.clear();
+  int ticket = 0;
+  // x of the next block: the call's input first, then the hidden-stream entry last written
+  int xsrc = g.embedding ? X_EMBED : X_HIDDEN_IN, x_idx = 0;
+  int prev = -1;  // op whose completion (all CTAs) makes x ready
+  auto blank = [&](int type) {
+    OpDesc o;
+    std::memset(&o, 0, sizeof(o));
+    o.type = type;
+    o.wait_ctr = o.wait2_ctr = o.pwait_ctr = -1;
+    o.sig_ctr = (int)ops.size();
+    o.xsrc = xsrc;
+    o.x_idx = x_idx;
+    o.x_src = c->embed;
+    o.slot1 = -1;
+    return o;
+  };
+  auto geom = [&](OpDesc& o) { tile_geometry(o.wtype, o.K, o.pair, o.tpr, o.rpt, o.unit); };
+  auto hs_at = [&](int idx) { return hs + (size_t)idx * M * H; };
+
+  for (int l = 0; l < g.n_layers; ++l) {
+    const LayerW& w = c->layers[l];
+    if (g.n_q) {
+      OpDesc q = blank(OP_QKV);
+      q.layer = l;
+      q.wtype = W_BF16;
+      q.N = qkv_rows;
+      q.K = H;
+      q.norm = 1;
+      q.gain = static_cast<const uint16_t*>(w.attn_norm);
+      q.w = w.wqkv;
+      q.out = wsp<float>(c, L.qkv) + (size_t)l * M * qkv_rows;
+      if (prev >= 0) { q.wait_ctr = prev; q.wait_n = C; }
+      geom(q);
+      const int qi = (int)ops.size();
+      ops.push_back(q);
+
+      OpDesc a = blank(OP_ATTN);
+      a.layer = l;
+      a.wait_ctr = qi;
+      a.wait_n = C;
+      a.act = q.out;
+      a.out = wsp<float>(c, L.attn_out) + (size_t)l * M * g.n_q * kHeadDim;
+      a.kc = c->kc + (size_t)l * g.n_kv * g.kv_capacity * kHeadDim;
+      a.vc = c->vc + (size_t)l * g.n_kv * g.kv_capacity * kHeadDim;
+      a.ticket = ticket;
+      ticket += g.n_kv;
+      const int ai = (int)ops.size();
+      ops.push_back(a);
+
+      OpDesc o = blank(OP_OPROJ);
+      o.layer = l;
+      o.wtype = W_BF16;
+      o.N = H;
+      o.K = g.n_q * kHeadDim;
+      o.w = w.wo;
+      o.act = a.out;
+      o.x_out = hs_at(2 * l + 1);
+      o.wait_ctr = ai;
+      o.wait_n = g.n_kv;
+      geom(o);
+      prev = (int)ops.size();
+      ops.push_back(o);
+      xsrc = X_F32;
+      x_idx = 2 * l + 1;
+    }
+    if (g.ffn) {
+      OpDesc u = blank(OP_GATEUP);
+      u.layer = l;
+      u.wtype = W_BF16;
+      u.N = 2 * g.ffn;
+      u.K = H;
+      u.pair = 1;
+      u.norm = 1;
+      u.gain = static_cast<const uint16_t*>(w.ffn_norm);
+      u.w = w.wgateup;
+      u.out = wsp<float>(c, L.hbuf) + (size_t)l * M * g.ffn;
+      if (prev >= 0) { u.wait_ctr = prev; u.wait_n = C; }
+      geom(u);
+      const int ui = (int)ops.size();
+      ops.push_back(u);
+
+      OpDesc d = blank(OP_DOWN);
+      d.layer = l;
+      d.wtype = W_BF16;
+      d.N = H;
+      d.K = g.ffn;
+      d.w = w.wdown;
+      d.act = u.out;
+      d.x_out = hs_at(2 * l + 2);
+      d.wait_ctr = ui;
+      d.wait_n = C;
+      geom(d);
+      prev = (int)ops.size();
+      ops.push_back(d);
+      xsrc = X_F32;
+      x_idx = 2 * l + 2;
+    }
+    if (g.n_experts) {
+      const int I = g.moe_inter, E = g.n_experts;
+      int32_t* route = reinterpret_cast<int32_t*>(wsp<uint8_t>(c, L.route) + (size_t)l * sizeof(RouteBlock));
+      float* eh = wsp<float>(c, L.eh) + (size_t)l * kMaxRouteSlots * M * I;
+      const int64_t gu_v = (int64_t)2 * I * (H / 2), gu_s = (int64_t)2 * I * (H / 32);
+      const int64_t dn_v = (int64_t)H * (I / 2), dn_s = (int64_t)H * (I / 32);
+
+      OpDesc r = blank(OP_ROUTER);
+      r.layer = l;
+      r.wtype = W_BF16;
+      r.N = E;
+      r.K = H;
+      r.norm = 1;
+      r.gain = static_cast<const uint16_t*>(w.ffn_norm);
+      r.w = w.wrouter;
+      r.out = wsp<float>(c, L.rlogits) + (size_t)l * M * E;
+      r.route = route;
+      r.ticket = ticket++;
+      if (prev >= 0) { r.wait_ctr = prev; r.wait_n = C; }
+      geom(r);
+      const int ri = (int)ops.size();
+      ops.push_back(r);
+
+      int si = -1;
+      if (g.n_shared) {
+        OpDesc sg = blank(OP_SHARED_GATEUP);
+        sg.layer = l;
+        sg.wtype = W_MXFP4;
+        sg.N = 2 * I;
+        sg.K = H;
+        sg.pair = 1;
+        sg.norm = 1;
+        sg.gain = static_cast<const uint16_t*>(w.ffn_norm);
+        sg.w = w.egu_v;
+        sg.ws = w.egu_s;
+        sg.w_mstride = gu_v;
+        sg.ws_mstride = gu_s;
+        sg.slot0 = 0;
+        sg.slot1 = g.n_shared;
+        sg.eh = eh;
+        sg.route = route;
+        if (prev >= 0) { sg.wait_ctr = prev; sg.wait_n = C; }
+        geom(sg);
+        si = (int)ops.size();
+        ops.push_back(sg);
+      }
+      OpDesc rg = blank(OP_ROUTED_GATEUP);
+      rg.layer = l;
+      rg.wtype = W_MXFP4;
+      rg.N = 2 * I;
+      rg.K = H;
+      rg.pair = 1;
+      rg.norm = 1;
+      rg.gain = static_cast<const uint16_t*>(w.ffn_norm);
+      rg.w = w.egu_v;
+      rg.ws = w.egu_s;
+      rg.w_mstride = gu_v;
+      rg.ws_mstride = gu_s;
+      rg.slot0 = g.n_shared;
+      rg.slot1 = -1;
+      rg.eh = eh;
+      rg.route = route;
+      rg.wait_ctr = ri;
+      rg.wait_n = 1;
+      rg.pwait_ctr = ri;
+      rg.pwait_n = 1;
+      geom(rg);
+      const int rgi = (int)ops.size();
+      ops.push_back(rg);
+
+      OpDesc dn = blank(OP_EXP_DOWN);
+      dn.layer = l;
+      dn.wtype = W_MXFP4;
+      dn.N = H;
+      dn.K = I;
+      dn.w = w.edn_v;
+      dn.ws = w.edn_s;
+      dn.w_mstride = dn_v;
+      dn.ws_mstride = dn_s;
+      dn.eh = eh;
+      dn.route = route;
+      dn.x_out = hs_at(2 * l + 2);
+      dn.wait_ctr = rgi;
+      dn.wait_n = C;
+      if (si >= 0) { dn.wait2_ctr = si; dn.wait2_n = C; }
+      dn.pwait_ctr = ri;
+      dn.pwait_n = 1;
+      geom(dn);
+      prev = (int)ops.size();
+      ops.push_back(dn);
+      xsrc = X_F32;
+      x_idx = 2 * l + 2;
+    }
+  }
+  if (g.vocab) {
+    OpDesc h = blank(OP_LMHEAD);
+    h.wtype = g.lm_head_dtype == DEC_FP8_E4M3_ROWSCALE ? W_FP8 : W_BF16;
+    h.N = g.vocab;
+    h.K = H;
+    h.norm = g.final_norm ? 1 : 0;
+    h.gain = static_cast<const uint16_t*>(c->final_norm);
+    h.w = c->lm_v;
+    h.ws = c->lm_s;
+    h.out = wsp<float>(c, L.logits);
+    h.ticket = ticket++;
+    h.sig_ctr = -1;
+    if (prev >= 0) { h.wait_ctr = prev; h.wait_n = C; }
+    geom(h);
+    ops.push_back(h);
+  }
+
+  KParams& k = c->kp;
+  std::memset(&k, 0, sizeof(k));
+  k.ops = wsp<OpDesc>(c, L.ops);
+  k.n_ops = (int)ops.size();
+  k.op_begin = 0;
+  k.op_end = k.n_ops;
+  k.n_ctas = C;
+  k.H = H;
+  k.n_q = g.n_q;
+  k.n_kv = g.n_kv;
+  k.G = g.n_q ? g.n_q / g.n_kv : 1;
+  k.qkv_rows = qkv_rows;
+  k.E = g.n_experts;
+  k.top_k = g.top_k;
+  k.I = g.moe_inter;
+  k.n_shared = g.n_shared;
+  k.V = g.vocab;
+  k.cap = g.kv_capacity;
+  k.Mmax = M;
+  k.L = g.n_layers;
+  k.ns_max = L.ns_max;
+  k.eps = g.rms_eps;
+  k.rope_base = g.rope_base;
+  k.timeout_ns = g.spin_timeout_ns ? g.spin_timeout_ns : 2000000000ull;
+  k.nslot = L.nslot;
+  k.act_bytes = L.act_bytes;
+  k.state = wsp<StepState>(c, L.state);
+  k.status = wsp<Status>(c, L.status);
+  k.ctr = wsp<uint32_t>(c, L.ctr);
+  k.tickets = wsp<uint32_t>(c, L.tickets);
+  k.part = wsp<float>(c, L.part);
+  k.am_val = wsp<float>(c, L.am_val);
+  k.am_idx = wsp<int32_t>(c, L.am_idx);
+  k.am_out = wsp<int32_t>(c, L.am_out);
+  k.step_ticket = ticket++;
+  k.hs = hs;
+}
+
+dec_status prepare(dec_ctx* c) {
+  if (c->sticky) return fail(DEC_ERR_STATE, "a device error is pending (code %d): call dec_reset", (int)c->sticky_code);
+  if (!c->ops_dirty) return DEC_OK;
+  dec_status st = check_weights(c);
+  if (st != DEC_OK) return st;
+  build_ops(c);
+  CUDA_TRY(cudaMemcpyAsync(c->ws + c->lay.ops, c->ops.data(), c->ops.size() * sizeof(OpDesc), cudaMemcpyHostToDevice,
+                           c->stream));
+  CUDA_TRY(cudaStreamSynchronize(c->stream));
+  if (c->graph) {
+    cudaGraphExecDestroy(c->graph);
+    c->graph = nullptr;
+  }
+  c->ops_dirty = false;
+  return DEC_OK;
+}
+
+dec_status launch_step(dec_ctx* c) {
+  KParams k = c->kp;
+  const dec_mode mode = c->cfg.mode;
+  if (mode == DEC_MODE_PERSISTENT) {
+    CUDA_TRY(dec_launch_megakernel(&k, 1, c->stream));
+    c->last_launches = 1;
+    return DEC_OK;
+  }
+  if (mode == DEC_MODE_PER_OP_GRAPH) {
+    if (!c->graph) {
+      cudaGraph_t g;
+      CUDA_TRY(cudaStreamBeginCapture(c->stream, cudaStreamCaptureModeThreadLocal));
+      cudaError_t err = cudaSuccess;
+      for (int i = 0; i < k.n_ops && err == cudaSuccess; ++i) {
+        KParams ki = k;
+        ki.op_begin = i;
+        ki.op_end = i + 1;
+        err = dec_launch_megakernel(&ki, 0, c->stream);
+      }
+      cudaError_t e2 = cudaStreamEndCapture(c->stream, &g);
+      if (err != cudaSuccess) return fail(DEC_ERR_CUDA, "graph capture launch: %s", cudaGetErrorString(err));
+      if (e2 != cudaSuccess) return fail(DEC_ERR_CUDA, "graph capture: %s", cudaGetErrorString(e2));
+      CUDA_TRY(cudaGraphInstantiate(&c->graph, g, 0));
+      cudaGraphDestroy(g);
+    }
+    CUDA_TRY(cudaGraphLaunch(c->graph, c->stream));
+    c->last_launches = k.n_ops;
+    return DEC_OK;
+  }
+  for (int i = 0; i < k.n_ops; ++i) {
+    KParams ki = k;
+    ki.op_begin = i;
+    ki.op_end = i + 1;
+    CUDA_TRY(dec_launch_megakernel(&ki, 0, c->stream));
+  }
+  c->last_launches = k.n_ops;
+  return DEC_OK;
+}
+
+// Host-written part of the step state (everything after `epoch`, which the device owns).
+dec_status write_state(dec_ctx* c, int32_t pos, int m, const int32_t* tokens, const void* hidden, int chain,
+                       int32_t* gen_out) {
+  StepState s;
+  std::memset(&s, 0, sizeof(s));
+  s.pos = pos;
+  s.m = m;
+  s.chain = chain;
+  for (int i = 0; i < m; ++i) s.tokens[i] = tokens ? tokens[i] : 0;
+  s.hidden_in = hidden;
+  s.gen_out = gen_out;
+  s.gen_idx = 0;
+  const size_t off = offsetof(StepState, pos);
+  CUDA_TRY(cudaMemcpyAsync(c->ws + c->lay.state + off, reinterpret_cast<const uint8_t*>(&s) + off,
+                           sizeof(StepState) - off, cudaMemcpyHostToDevice, c->stream));
+  return DEC_OK;
+}
+
+dec_status read_status(dec_ctx* c) {
+  Status s;
+  CUDA_TRY(cudaMemcpyAsync(&s, c->ws + c->lay.status, sizeof(s), cudaMemcpyDeviceToHost, c->stream));
+  CUDA_TRY(cudaStreamSynchronize(c->stream));
+  if (s.code != 0) {
+    c->sticky = true;
+    c->sticky_code = (dec_status)s.code;
+    return fail((dec_status)s.code, "device wait timed out: op %d, cta %d, counter %u observed %u target %u (site %u)",
+                s.op, s.cta, s.counter, s.observed, s.target, s.where);
+  }
+  return DEC_OK;
+}
+
+dec_status check_call(dec_ctx* c, int32_t pos, int m, const int32_t* tokens, const void* hidden) {
+  const dec_config& g = c->cfg;
+  if (m < 1 || m > g.max_verify) return fail(DEC_ERR_INVALID_ARG, "window of %d tokens (max_verify %d)", m, g.max_verify);
+  if (pos < 0) return fail(DEC_ERR_INVALID_ARG, "negative position");
+  if (g.n_q && (long long)pos + m > g.kv_capacity)
+    return fail(DEC_ERR_CAPACITY, "positions %d..%d exceed kv_capacity %d", pos, pos + m - 1, g.kv_capacity);
+  if (g.embedding) {
+    if (!tokens) return fail(DEC_ERR_INVALID_ARG, "tokens required");
+    for (int i = 0; i < m; ++i)
+      if (tokens[i] < 0 || tokens[i] >= g.vocab) return fail(DEC_ERR_CAPACITY, "token %d outside the vocabulary", tokens[i]);
+  } else if (g.n_layers > 0 || g.vocab) {
+    if (!hidden) return fail(DEC_ERR_INVALID_ARG, "hidden_dev required (config without embedding)");
+    if (reinterpret_cast<uintptr_t>(hidden) % 16) return fail(DEC_ERR_INVALID_ARG, "hidden_dev must be 16-byte aligned");
+  }
+  return DEC_OK;
+}
+
+dec_status run_call(dec_ctx* c, int32_t pos, int m, const int32_t* tokens, const void* hidden, float* logits_dev,
+                    int32_t* argmax_host) {
+  dec_status st = prepare(c);
+  if (st != DEC_OK) return st;
+  st = check_call(c, pos, m, tokens, hidden);
+  if (st != DEC_OK) return st;
+  st = write_state(c, pos, m, tokens, hidden, 0, nullptr);
+  if (st != DEC_OK) return st;
+  st = launch_step(c);
+  if (st != DEC_OK) return st;
+  if (logits_dev && c->cfg.vocab)
+    CUDA_TRY(cudaMemcpyAsync(logits_dev, c->ws + c->lay.logits, (size_t)m * c->cfg.vocab * 4, cudaMemcpyDeviceToDevice,
+                             c->stream));
+  if (argmax_host) {
+    CUDA_TRY(cudaMemcpyAsync(argmax_host, c->ws + c->lay.am_out, (size_t)m * 4, cudaMemcpyDeviceToHost, c->stream));
+    return read_status(c);
+  }
+  return DEC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* dec_last_error(void) { return g_last_error.c_str(); }
+
+size_t dec_workspace_bytes(const dec_config* cfg) {
+  std::string why;
+  if (!validate(cfg, why)) {
+    fail(DEC_ERR_INVALID_ARG, "invalid config: %s", why.c_str());
+    return 0;
+  }
+  Layout L;
+  if (!compute_layout(cfg, L, why)) {
+    fail(DEC_ERR_SHAPE, "%s", why.c_str());
+    return 0;
+  }
+  return L.total;
+}
+
+dec_status dec_init(const dec_config* cfg, void* cuda_stream, void* workspace_dev, dec_ctx** out) {
+  if (!out) return fail(DEC_ERR_INVALID_ARG, "out is null");
+  *out = nullptr;
+  std::string why;
+  if (!validate(cfg, why)) return fail(DEC_ERR_INVALID_ARG, "invalid config: %s", why.c_str());
+  if (!workspace_dev) return fail(DEC_ERR_INVALID_ARG, "workspace is null");
+  if (reinterpret_cast<uintptr_t>(workspace_dev) % 256) return fail(DEC_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  Layout L;
+  if (!compute_layout(cfg, L, why)) return fail(DEC_ERR_SHAPE, "%s", why.c_str());
+  dec_ctx* c = new dec_ctx();
+  c->cfg = *cfg;
+  c->stream = static_cast<cudaStream_t>(cuda_stream);
+  c->ws = static_cast<uint8_t*>(workspace_dev);
+  c->lay = L;
+  c->layers.resize(cfg->n_layers);
+  cudaError_t e = cudaMemsetAsync(c->ws, 0, L.total, c->stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);
+  if (e != cudaSuccess) {
+    delete c;
+    return fail(DEC_ERR_CUDA, "clearing the workspace: %s", cudaGetErrorString(e));
+  }
+  *out = c;
+  return DEC_OK;
+}
+
+dec_status dec_load_weights(dec_ctx* c, const dec_tensor* t, int n) {
+  if (!c || (!t && n > 0) || n < 0) return fail(DEC_ERR_INVALID_ARG, "null context or tensors");
+  const dec_config& g = c->cfg;
+  const int H = g.hidden;
+  for (int i = 0; i < n; ++i) {
+    const dec_tensor& x = t[i];
+    if (!x.values || reinterpret_cast<uintptr_t>(x.values) % 16)
+      return fail(DEC_ERR_INVALID_ARG, "tensor %d: values null or not 16-byte aligned", i);
+    const bool head = x.kind == DEC_T_EMBED || x.kind == DEC_T_FINAL_NORM || x.kind == DEC_T_LM_HEAD;
+    if (!head && (x.layer < 0 || x.layer >= g.n_layers)) return fail(DEC_ERR_SHAPE, "tensor %d: layer %d", i, x.layer);
+    auto want = [&](dec_dtype dt, int r, int cc) -> dec_status {
+      if (x.dtype != dt) return fail(DEC_ERR_DTYPE, "tensor %d (kind %d): dtype %d, expected %d", i, x.kind, x.dtype, dt);
+      if (x.rows != r || x.cols != cc)
+        return fail(DEC_ERR_SHAPE, "tensor %d (kind %d): shape %dx%d, expected %dx%d", i, x.kind, x.rows, x.cols, r, cc);
+      if (dt != DEC_BF16 && (!x.scales || reinterpret_cast<uintptr_t>(x.scales) % 16))
+        return fail(DEC_ERR_INVALID_ARG, "tensor %d: scales null or not 16-byte aligned", i);
+      return DEC_OK;
+    };
+    dec_status st = DEC_OK;
+    LayerW* w = head ? nullptr : &c->layers[x.layer];
+    const int qkv_rows = (g.n_q + 2 * g.n_kv) * kHeadDim;
+    switch (x.kind) {
+      case DEC_T_EMBED:
+        if (!g.embedding) return fail(DEC_ERR_STATE, "config has no embedding");
+        st = want(DEC_BF16, g.vocab, H);
+        if (st == DEC_OK) c->embed = x.values;
+        break;
+      case DEC_T_ATTN_NORM:
+      case DEC_T_FFN_NORM:
+      case DEC_T_FINAL_NORM:
+        if (x.rows * x.cols != H || x.dtype != DEC_BF16) return fail(DEC_ERR_SHAPE, "tensor %d: a norm gain is bf16 [H]", i);
+        if (x.kind == DEC_T_ATTN_NORM) w->attn_norm = x.values;
+        else if (x.kind == DEC_T_FFN_NORM) w->ffn_norm = x.values;
+        else c->final_norm = x.values;
+        break;
+      case DEC_T_WQKV:
+        if (!g.n_q) return fail(DEC_ERR_STATE, "config has no attention");
+        st = want(DEC_BF16, qkv_rows, H);
+        if (st == DEC_OK) w->wqkv = x.values;
+        break;
+      case DEC_T_WO:
+        if (!g.n_q) return fail(DEC_ERR_STATE, "config has no attention");
+        st = want(DEC_BF16, H, g.n_q * kHeadDim);
+        if (st == DEC_OK) w->wo = x.values;
+        break;
+      case DEC_T_WGATEUP:
+        if (!g.ffn) return fail(DEC_ERR_STATE, "config has no dense FFN");
+        st = want(DEC_BF16, 2 * g.ffn, H);
+        if (st == DEC_OK) w->wgateup = x.values;
+        break;
+      case DEC_T_WDOWN:
+        if (!g.ffn) return fail(DEC_ERR_STATE, "config has no dense FFN");
+        st = want(DEC_BF16, H, g.ffn);
+        if (st == DEC_OK) w->wdown = x.values;
+        break;
+      case DEC_T_WROUTER:
+        if (!g.n_experts) return fail(DEC_ERR_STATE, "config has no MoE");
+        st = want(DEC_BF16, g.n_experts, H);
+        if (st == DEC_OK) w->wrouter = x.values;
+        break;
+      case DEC_T_EXPERT_GATEUP:
+        if (!g.n_experts) return fail(DEC_ERR_STATE, "config has no MoE");
+        st = want(DEC_MXFP4, 2 * g.moe_inter, H);
+        if (st == DEC_OK) { w->egu_v = x.values; w->egu_s = x.scales; }
+        break;
+      case DEC_T_EXPERT_DOWN:
+        if (!g.n_experts) return fail(DEC_ERR_STATE, "config has no MoE");
+        st = want(DEC_MXFP4, H, g.moe_inter);
+        if (st == DEC_OK) { w->edn_v = x.values; w->edn_s = x.scales; }
+        break;
+      case DEC_T_LM_HEAD:
+        if (!g.vocab) return fail(DEC_ERR_STATE, "config has no LM head");
+        st = want(g.lm_head_dtype, g.vocab, H);
+        if (st == DEC_OK) { c->lm_v = x.values; c->lm_s = x.scales; }
+        break;
+      default:
+        return fail(DEC_ERR_INVALID_ARG, "tensor %d: unknown kind %d", i, (int)x.kind);
+    }
+    if (st != DEC_OK) return st;
+  }
+  c->ops_dirty = true;
+  return DEC_OK;
+}
+
+dec_status dec_set_kv_cache(dec_ctx* c, void* k_dev, void* v_dev) {
+  if (!c) return fail(DEC_ERR_INVALID_ARG, "null context");
+  if (!c->cfg.n_q) return fail(DEC_ERR_STATE, "config has no attention");
+  if (!k_dev || !v_dev || reinterpret_cast<uintptr_t>(k_dev) % 256 || reinterpret_cast<uintptr_t>(v_dev) % 256)
+    return fail(DEC_ERR_INVALID_ARG, "KV cache pointers must be non-null and 256-byte aligned");
+  c->kc = static_cast<uint16_t*>(k_dev);
+  c->vc = static_cast<uint16_t*>(v_dev);
+  c->ops_dirty = true;
+  return DEC_OK;
+}
+
+dec_status dec_step(dec_ctx* c, int32_t token, const void* hidden_dev, int32_t pos, float* logits_dev,
+                    int32_t* argmax_host) {
+  if (!c) return fail(DEC_ERR_INVALID_ARG, "null context");
+  return run_call(c, pos, 1, &token, hidden_dev, logits_dev, argmax_host);
+}
+
+dec_status dec_verify(dec_ctx* c, const int32_t* tokens_host, const void* hidden_dev, int k, int32_t pos,
+                      float* logits_dev, int32_t* argmax_host, int32_t* n_accepted) {
+  if (!c) return fail(DEC_ERR_INVALID_ARG, "null context");
+  int32_t am[kMmax] = {0, 0, 0, 0};
+  const bool need_am = argmax_host || n_accepted;
+  dec_status st = run_call(c, pos, k, tokens_host, hidden_dev, logits_dev, need_am ? am : nullptr);
+  if (st != DEC_OK) return st;
+  if (argmax_host)
+    for (int i = 0; i < k; ++i) argmax_host[i] = am[i];
+  if (n_accepted) {
+    int j = 0;
+    while (tokens_host && j + 1 < k && tokens_host[j + 1] == am[j]) ++j;
+    *n_accepted = j + 1;
+  }
+  return DEC_OK;
+}
+
+dec_status dec_generate(dec_ctx* c, int32_t token, int32_t pos, int n, int32_t* tokens_dev) {
+  if (!c) return fail(DEC_ERR_INVALID_ARG, "null context");
+  if (n < 0) return fail(DEC_ERR_INVALID_ARG, "negative step count");
+  if (!c->cfg.embedding || !c->cfg.vocab) return fail(DEC_ERR_STATE, "chained generation needs an embedding and an LM head");
+  dec_status st = prepare(c);
+  if (st != DEC_OK) return st;
+  if (n == 0) return DEC_OK;
+  st = check_call(c, pos, 1, &token, nullptr);
+  if (st != DEC_OK) return st;
+  if (c->cfg.n_q && (long long)pos + n > c->cfg.kv_capacity)
+    return fail(DEC_ERR_CAPACITY, "positions %d..%d exceed kv_capacity %d", pos, pos + n - 1, c->cfg.kv_capacity);
+  st = write_state(c, pos, 1, &token, nullptr, 1, tokens_dev);
+  if (st != DEC_OK) return st;
+  int launches = 0;
+  for (int i = 0; i < n; ++i) {
+    st = launch_step(c);
+    if (st != DEC_OK) return st;
+    launches += c->last_launches;
+  }
+  c->last_launches = launches;
+  return DEC_OK;
+}
+
+dec_status dec_debug_buffers(dec_ctx* c, const float** hidden, const float** qkv, const int32_t** routing) {
+  if (!c) return fail(DEC_ERR_INVALID_ARG, "null context");
+  if (hidden) *hidden = wsp<float>(c, c->lay.hs);
+  if (qkv) *qkv = wsp<float>(c, c->lay.qkv);
+  if (routing) *routing = reinterpret_cast<const int32_t*>(c->ws + c->lay.route);
+  return DEC_OK;
+}
+
+dec_status dec_reset(dec_ctx* c) {
+  if (!c) return fail(DEC_ERR_INVALID_ARG, "null context");
+  // counters, tickets, status and the device-owned epoch restart from zero
+  CUDA_TRY(cudaStreamSynchronize(c->stream));
+  CUDA_TRY(cudaMemsetAsync(c->ws + c->lay.state, 0, c->lay.ops - c->lay.state, c->stream));
+  CUDA_TRY(cudaStreamSynchronize(c->stream));
+  c->sticky = false;
+  c->sticky_code = DEC_OK;
+  return DEC_OK;
+}
+
+dec_status dec_sync(dec_ctx* c) {
+  if (!c) return fail(DEC_ERR_INVALID_ARG, "null context");
+  if (c->sticky) return fail(DEC_ERR_STATE, "a device error is pending (code %d): call dec_reset", (int)c->sticky_code);
+  return read_status(c);
+}
+
+int dec_last_launch_count(dec_ctx* c) { return c ? c->last_launches : 0; }
+
+void dec_free(dec_ctx* c) {
+  if (!c) return;
+  if (c->graph) cudaGraphExecDestroy(c->graph);
+  delete c;
+}
+
+}  // extern "C"

@@ -1,0 +1,232 @@
+"""Load a model into the library: pack weights, place them in device memory, register them.
+
+PyTorch is used for device memory and the stream only; every step of the decode runs in the
+library's kernels. Weights arrive as logical bfloat16 bits (numpy ``uint16``, matrices
+[out_features, in_features]); packing follows ``dec_pack`` / ``dec_pack_pair``.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+import torch
+
+from . import binding as B
+
+_DTYPE = {"bf16": B.DEC_BF16, "fp8": B.DEC_FP8_E4M3_ROWSCALE, "mxfp4": B.DEC_MXFP4}
+_MODE = {"persistent": B.DEC_MODE_PERSISTENT, "per_op": B.DEC_MODE_PER_OP, "graph": B.DEC_MODE_PER_OP_GRAPH}
+
+
+def make_config(shape, capacity: int, max_verify: int = 1, mode: str = "persistent", num_ctas: int = 0,
+                timeout_ns: int = 0) -> B.DecConfig:
+    c = B.DecConfig()
+    c.n_layers = shape.n_layers
+    c.hidden = shape.hidden
+    c.n_q = shape.n_q
+    c.n_kv = shape.n_kv
+    c.head_dim = shape.head_dim
+    c.ffn = shape.ffn
+    c.n_experts = shape.n_experts
+    c.top_k = shape.top_k
+    c.moe_inter = shape.moe_inter
+    c.n_shared = shape.n_shared
+    c.vocab = shape.vocab
+    c.kv_capacity = capacity
+    c.max_verify = max_verify
+    c.embedding = 1 if shape.embedding else 0
+    c.final_norm = 1 if shape.final_norm else 0
+    c.rms_eps = shape.rms_eps
+    c.rope_base = shape.rope_base
+    c.lm_head_dtype = _DTYPE[shape.lm_head_dtype]
+    c.expert_dtype = B.DEC_MXFP4
+    c.mode = _MODE[mode]
+    c.spin_timeout_ns = timeout_ns
+    c.num_ctas = num_ctas
+    return c
+
+
+def _dev(a: np.ndarray, device) -> torch.Tensor:
+    """numpy array -> device tensor with the same bytes (uint16 bits travel as int16)."""
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        a = a.view(np.int16)
+    return torch.from_numpy(a).to(device)
+
+
+def pack_host(dtype: int, w: np.ndarray, pair_with: np.ndarray | None = None):
+    """Pack one logical bf16 matrix (or two, interleaved row by row) on the host."""
+    rows, cols = w.shape
+    out_rows = rows * (2 if pair_with is not None else 1)
+    vb, sb = B.dec_packed_bytes(dtype, out_rows, cols)
+    vals = np.empty(vb, np.uint8)
+    scales = np.empty(max(sb, 1), np.uint8)
+    w = np.ascontiguousarray(w, dtype=np.uint16)
+    if pair_with is None:
+        B.dec_pack(dtype, w, rows, cols, vals, scales if sb else None)
+    else:
+        B.dec_pack_pair(dtype, w, np.ascontiguousarray(pair_with, dtype=np.uint16), rows, cols, vals,
+                        scales if sb else None)
+    return vals, (scales[:sb] if sb else None)
+
+
+class Decoder:
+    """One model instance on one GPU: workspace, packed weights, KV cache, context.
+
+    shape      : a ModelShape (dims, eps, RoPE base, head dtype, embedding)
+    layers     : per-layer dicts of logical bf16 weights (attn_norm, w_qkv, w_o, ffn_norm,
+                 w_gate, w_up, w_down, w_router)
+    head       : dict with embed / final_norm / w_lm
+    experts    : callable (layer, expert) -> (gate, up, down) bf16 for MoE layers; experts
+                 shape.n_experts .. + n_shared - 1 are the shared ones
+    kv         : list of (K, V) bf16 prefills [n_kv, n, d] per layer, or None
+    """
+
+    def __init__(self, shape, layers, head, experts=None, kv=None, capacity=None, max_verify=1, mode="persistent",
+                 num_ctas=0, timeout_ns=0, device="cuda:0", packed_experts=None):
+        self.shape = shape
+        self.device = torch.device(device)
+        # a stream of its own: CUDA-graph capture cannot use the legacy default stream
+        self.stream = torch.cuda.Stream(self.device)
+        self.capacity = capacity if capacity is not None else max(1, shape.kv_prefill + 8)
+        self.max_verify = max_verify
+        self.cfg = make_config(shape, self.capacity, max_verify, mode, num_ctas, timeout_ns)
+        nbytes = B.dec_workspace_bytes(self.cfg)
+        if nbytes == 0:
+            raise B.DecError(B.DEC_ERR_INVALID_ARG, B.dec_last_error())
+        self.workspace = torch.zeros(nbytes + 256, dtype=torch.uint8, device=self.device)
+        off = (-self.workspace.data_ptr()) % 256
+        self.ws = self.workspace[off:off + nbytes]
+        torch.cuda.synchronize(self.device)
+        self.ctx = B.dec_init(self.cfg, self.stream.cuda_stream, self.ws)
+        self._keep = []
+        tensors = []
+
+        def reg(kind, layer, dtype, rows, cols, vals, scales=None):
+            v = vals if isinstance(vals, torch.Tensor) else _dev(vals, self.device)
+            s = None if scales is None else (scales if isinstance(scales, torch.Tensor) else _dev(scales, self.device))
+            self._keep += [v, s]
+            tensors.append(B.DecTensor(kind, layer, dtype, rows, cols, v.data_ptr(),
+                                       s.data_ptr() if s is not None else None))
+
+        s = shape
+        H = s.hidden
+        for l, w in enumerate(layers):
+            if s.attn:
+                reg(B.DEC_T_ATTN_NORM, l, B.DEC_BF16, H, 1, w["attn_norm"])
+                reg(B.DEC_T_WQKV, l, B.DEC_BF16, s.qkv_rows, H, w["w_qkv"])
+                reg(B.DEC_T_WO, l, B.DEC_BF16, H, s.n_q * s.head_dim, w["w_o"])
+            if s.ffn or s.moe:
+                reg(B.DEC_T_FFN_NORM, l, B.DEC_BF16, H, 1, w["ffn_norm"])
+            if s.ffn:
+                vals, _ = pack_host(B.DEC_BF16, w["w_gate"], w["w_up"])
+                reg(B.DEC_T_WGATEUP, l, B.DEC_BF16, 2 * s.ffn, H, vals)
+                reg(B.DEC_T_WDOWN, l, B.DEC_BF16, H, s.ffn, w["w_down"])
+            if s.moe:
+                reg(B.DEC_T_WROUTER, l, B.DEC_BF16, s.n_experts, H, w["w_router"])
+                if packed_experts is not None:
+                    gu_v, gu_s, dn_v, dn_s = packed_experts(l)
+                else:
+                    gu_v, gu_s, dn_v, dn_s = self._pack_experts(experts, l)
+                reg(B.DEC_T_EXPERT_GATEUP, l, B.DEC_MXFP4, 2 * s.moe_inter, H, gu_v, gu_s)
+                reg(B.DEC_T_EXPERT_DOWN, l, B.DEC_MXFP4, H, s.moe_inter, dn_v, dn_s)
+        if s.embedding:
+            reg(B.DEC_T_EMBED, 0, B.DEC_BF16, s.vocab, H, head["embed"])
+        if s.vocab:
+            if s.final_norm:
+                reg(B.DEC_T_FINAL_NORM, 0, B.DEC_BF16, H, 1, head["final_norm"])
+            if s.lm_head_dtype == "fp8":
+                vals, scales = pack_host(B.DEC_FP8_E4M3_ROWSCALE, head["w_lm"])
+                reg(B.DEC_T_LM_HEAD, 0, B.DEC_FP8_E4M3_ROWSCALE, s.vocab, H, vals, scales)
+            else:
+                reg(B.DEC_T_LM_HEAD, 0, B.DEC_BF16, s.vocab, H, head["w_lm"])
+        B.dec_load_weights(self.ctx, tensors)
+
+        if s.attn:
+            self.k_cache = torch.zeros((s.n_layers, s.n_kv, self.capacity, s.head_dim), dtype=torch.int16,
+                                       device=self.device)
+            self.v_cache = torch.zeros_like(self.k_cache)
+            if kv is not None:
+                for l, (k, v) in enumerate(kv):
+                    n = k.shape[1]
+                    self.k_cache[l, :, :n] = _dev(k, self.device)
+                    self.v_cache[l, :, :n] = _dev(v, self.device)
+            B.dec_set_kv_cache(self.ctx, self.k_cache, self.v_cache)
+        torch.cuda.synchronize(self.device)
+        self.logits = torch.empty((max_verify, max(s.vocab, 1)), dtype=torch.float32, device=self.device)
+
+    def _pack_experts(self, experts, l):
+        s = self.shape
+        n = s.n_experts + s.n_shared
+        H, I = s.hidden, s.moe_inter
+        gu_v = np.empty((n, 2 * I * H // 2), np.uint8)
+        gu_s = np.empty((n, 2 * I * H // 32), np.uint8)
+        dn_v = np.empty((n, H * I // 2), np.uint8)
+        dn_s = np.empty((n, H * I // 32), np.uint8)
+        for e in range(n):
+            g, u, d = experts(l, e)
+            B.dec_pack_pair(B.DEC_MXFP4, np.ascontiguousarray(g), np.ascontiguousarray(u), I, H, gu_v[e], gu_s[e])
+            B.dec_pack(B.DEC_MXFP4, np.ascontiguousarray(d), H, I, dn_v[e], dn_s[e])
+        return gu_v, gu_s, dn_v, dn_s
+
+    # ------------------------------------------------------------------ calls
+    def _order(self):
+        # inputs written on the caller's stream must land before the library's stream reads them
+        self.stream.wait_stream(torch.cuda.current_stream(self.device))
+
+    def step(self, token: int = 0, pos: int = 0, hidden: torch.Tensor | None = None, logits: bool = True) -> int:
+        self._order()
+        return B.dec_step(self.ctx, token, hidden, pos, self.logits if logits else None)
+
+    def verify(self, tokens, pos: int, hidden: torch.Tensor | None = None, k: int | None = None):
+        self._order()
+        k = k if k is not None else len(tokens)
+        return B.dec_verify(self.ctx, tokens, hidden, k, pos, self.logits)
+
+    def generate(self, token: int, pos: int, n: int, out: torch.Tensor | None = None) -> torch.Tensor:
+        out = out if out is not None else torch.empty(n, dtype=torch.int32, device=self.device)
+        self._order()
+        B.dec_generate(self.ctx, token, pos, n, out)
+        return out
+
+    def sync(self):
+        B.dec_sync(self.ctx)
+        torch.cuda.current_stream(self.device).wait_stream(self.stream)
+
+    def reset(self):
+        B.dec_reset(self.ctx)
+
+    def launches(self) -> int:
+        return B.dec_last_launch_count(self.ctx)
+
+    def hidden_stream(self) -> torch.Tensor:
+        """fp32 [2L + 1, max_verify, H] view of the residual stream of the last call."""
+        h, _, _ = B.dec_debug_buffers(self.ctx)
+        s = self.shape
+        n = (2 * s.n_layers + 1) * self.max_verify * s.hidden
+        off = h - self.ws.data_ptr()
+        return self.ws[off:off + 4 * n].view(torch.float32).view(2 * s.n_layers + 1, self.max_verify, s.hidden)
+
+    def routing(self, layer: int) -> dict:
+        """Routing block of a MoE layer after the last call (slots, per-token top-k)."""
+        _, _, r = B.dec_debug_buffers(self.ctx)
+        off = r - self.ws.data_ptr()
+        sz = 4 * (1 + 33 + 4 * 33 + 4 * 8 + 4 * 8)
+        raw = self.ws[off + layer * sz: off + (layer + 1) * sz].cpu().numpy()
+        i32 = raw.view(np.int32)
+        f32 = raw.view(np.float32)
+        n = int(i32[0])
+        return {"n_slots": n, "expert": i32[1:1 + n].tolist(),
+                "w": f32[34:34 + 4 * 33].reshape(4, 33)[:, :n],
+                "topk": i32[34 + 132: 34 + 132 + 32].reshape(4, 8),
+                "topk_w": f32[34 + 132 + 32: 34 + 132 + 64].reshape(4, 8)}
+
+    def close(self):
+        if self.ctx:
+            B.dec_free(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

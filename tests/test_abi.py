@@ -1,0 +1,125 @@
+"""The C ABI library without a GPU: it loads, exports every symbol include/dec.h declares,
+rejects bad configs and calls on the host, and its packer writes exactly the bytes of the
+oracle's own quantisers (integer work: bit-exact)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import synth
+from oracle import formats as F
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="session")
+def B():
+    from persistent_megakernel_gb300 import build
+    build.build()
+    from persistent_megakernel_gb300 import binding
+    binding.lib()
+    return binding
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "dec.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dec_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(B):
+    names = _declared()
+    assert len(names) >= 16
+    lib = ctypes.CDLL(B.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(B.EXPORTS) == names
+
+
+def test_struct_layouts_match_header(B):
+    # dec_config: 15 ints, 2 floats, 3 enums, a uint64 (8-aligned), an int -> 96 bytes
+    assert ctypes.sizeof(B.DecConfig) == 96
+    assert B.DecConfig.spin_timeout_ns.offset == 80
+    assert ctypes.sizeof(B.DecTensor) == 40 and B.DecTensor.values.offset == 24
+
+
+def _cfg(B, **kw):
+    c = B.DecConfig()
+    base = dict(n_layers=1, hidden=256, n_q=4, n_kv=2, head_dim=128, ffn=512, vocab=100, kv_capacity=64, max_verify=1,
+                embedding=1, final_norm=1, rms_eps=1e-6, rope_base=1e4, num_ctas=8)
+    base.update(kw)
+    for k, v in base.items():
+        setattr(c, k, v)
+    return c
+
+
+def test_workspace_bytes_and_config_validation(B):
+    assert B.dec_workspace_bytes(_cfg(B)) > 0
+    bad = [dict(hidden=100), dict(head_dim=64), dict(n_kv=3), dict(max_verify=5), dict(ffn=12),
+           dict(n_q=32, n_kv=2), dict(ffn=0, n_experts=8, top_k=9, moe_inter=64), dict(embedding=1, vocab=0),
+           dict(ffn=0, n_experts=8, top_k=2, moe_inter=48), dict(mode=7)]
+    for b in bad:
+        assert B.dec_workspace_bytes(_cfg(B, **b)) == 0, b
+        assert "invalid config" in B.dec_last_error()
+
+
+def test_init_rejects_bad_arguments(B):
+    out = ctypes.c_void_p()
+    L = B.lib()
+    assert L.dec_init(ctypes.byref(_cfg(B)), None, None, ctypes.byref(out)) == B.DEC_ERR_INVALID_ARG
+    assert L.dec_init(ctypes.byref(_cfg(B)), None, 0x1001, ctypes.byref(out)) == B.DEC_ERR_INVALID_ARG
+    assert "aligned" in B.dec_last_error()
+    assert L.dec_init(ctypes.byref(_cfg(B, hidden=96)), None, 0x1000, ctypes.byref(out)) == B.DEC_ERR_INVALID_ARG
+    assert L.dec_step(None, 0, None, 0, None, None) == B.DEC_ERR_INVALID_ARG
+    assert L.dec_reset(None) == B.DEC_ERR_INVALID_ARG
+
+
+def test_packed_bytes(B):
+    assert B.dec_packed_bytes(B.DEC_BF16, 3, 16) == (96, 0)
+    assert B.dec_packed_bytes(B.DEC_FP8_E4M3_ROWSCALE, 3, 32) == (96, 12)
+    assert B.dec_packed_bytes(B.DEC_MXFP4, 4, 64) == (128, 8)
+    with pytest.raises(B.DecError):
+        B.dec_packed_bytes(B.DEC_MXFP4, 4, 48)
+
+
+def test_fp8_packer_equals_oracle_quantiser(B):
+    w = synth.normal_bf16(3, 501, (64, 2560), 0.0, 0.02)
+    w[5] = 0
+    w[6, :] = 0x8000                                   # negative zeros
+    w[7, 3] = 0x4480                                   # 1024.0: a large outlier
+    vals = np.empty(64 * 2560, np.uint8)
+    scales = np.empty(64, np.float32)
+    B.dec_pack(B.DEC_FP8_E4M3_ROWSCALE, w, 64, 2560, vals, scales)
+    codes, s = F.quantize_fp8_rows(w)
+    assert np.array_equal(s, scales)
+    assert np.array_equal(codes.reshape(-1), vals)
+
+
+def test_mxfp4_packer_equals_oracle_quantiser(B):
+    w = synth.normal_bf16(4, 502, (48, 768), 0.0, 0.02)
+    w[1, 32:64] = 0
+    w[2, 0] = 0x0001                                   # bf16 subnormal
+    w[3, 64:96] = synth.normal_bf16(4, 503, 32, 0.0, 1e-30)   # tiny block
+    vals = np.empty(48 * 384, np.uint8)
+    scales = np.empty(48 * 24, np.uint8)
+    B.dec_pack(B.DEC_MXFP4, w, 48, 768, vals, scales)
+    codes, e = F.quantize_mxfp4(w)
+    assert np.array_equal(e.reshape(-1), scales)
+    assert np.array_equal(codes.reshape(-1), vals)
+
+
+def test_pair_packer_interleaves_rows(B):
+    a = synth.normal_bf16(5, 504, (6, 64), 0.0, 0.02)
+    b = synth.normal_bf16(5, 505, (6, 64), 0.0, 0.02)
+    vals = np.empty(12 * 32, np.uint8)
+    sc = np.empty(12 * 2, np.uint8)
+    B.dec_pack_pair(B.DEC_MXFP4, a, b, 6, 64, vals, sc)
+    inter = np.empty((12, 64), np.uint16)
+    inter[0::2], inter[1::2] = a, b
+    codes, e = F.quantize_mxfp4(inter)
+    assert np.array_equal(codes.reshape(-1), vals) and np.array_equal(e.reshape(-1), sc)
+    out = np.empty(12 * 64, np.uint16)
+    B.dec_pack_pair(B.DEC_BF16, a, b, 6, 64, out, None)
+    assert np.array_equal(out.reshape(12, 64), inter)
