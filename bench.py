@@ -1,0 +1,339 @@
+"""Benchmark: batch-1 greedy decode of the 2B-class dense decoder on one GB300 per rank.
+
+Workload (the 2B dense config): 28 layers, hidden 2560, GQA 20 q / 4 kv heads of dim 128,
+SwiGLU 6912, vocabulary 32768, bf16 weights ~N(0, 0.02) (random init, seeded), bf16 KV cache
+prefilled to 4096 positions ~N(0, 1), greedy steps from a seeded token. A step is one whole
+decode step (embedding row, 28 layers of RMSNorm / QKV / RoPE + KV append / attention /
+o-proj / SwiGLU FFN, final norm, LM head, argmax) -- one launch of the persistent
+megakernel. Steps run in chains of 256 (positions 4096..4351, the workload's 256 greedy
+steps), repeated until K steps are timed.
+
+Prints ONE JSON line (rank 0). Multi-GPU runs are replicas: every rank decodes its own
+request on its own GPU with no communication on the data path; value = all ranks' tokens /
+the slowest rank's time (weak scaling). ``--impl reference`` times the CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "batch-1 decode tokens/s and achieved HBM GB/s (fraction of GB300 peak)"
+CHAIN = 256          # greedy steps of the workload, positions 4096 .. 4351
+NOMINAL_HBM_GBS = 8000.0
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def dist_setup(n_gpus):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws > 1:
+        import torch
+        import torch.distributed as dist
+        local = int(os.environ.get("LOCAL_RANK", "0"))
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+        return dist.get_rank(), ws, local
+    return 0, 1, 0
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, ws: int) -> float:
+    if ws == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+class Clocks:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}", "--format=csv",
+                                          "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for ln in open(self.path).read().splitlines()[1:]:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append((float(f[1].split()[0]), float(f[2].split()[0]), f[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def ncu_traffic(name: str, source_files):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged."""
+    p = os.path.join(ROOT, "profiles", name)
+    if not os.path.exists(p):
+        return None
+    txt = open(p).read()
+    m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    h = re.search(r"source_sha256:\s*([0-9a-f]+)", txt)
+    if not m or not h:
+        return None
+    sha = hashlib.sha256()
+    for f in source_files:
+        sha.update(open(f, "rb").read())
+    return float(m.group(1)) if sha.hexdigest() == h.group(1) else None
+
+
+def kernel_sources():
+    c = os.path.join(ROOT, "persistent_megakernel_gb300", "csrc")
+    return [os.path.join(c, f) for f in ("megakernel.cu", "gemv.cuh", "ptx.cuh", "dec_internal.h")]
+
+
+def build_workload(seed: int, layers: int = 0):
+    import synth
+    from synth import model as sm
+    s = synth.dense_2b_shape()
+    if layers:
+        s = s.with_(n_layers=layers)
+    layers = [sm.layer_weights(s, seed, l) for l in range(s.n_layers)]
+    head = sm.head_weights(s, seed)
+    kv = [sm.kv_prefill(s, seed, l) for l in range(s.n_layers)]
+    return s, layers, head, kv
+
+
+def cpu_baseline(s, layers, head, kv, seed):
+    """The oracle as it stands, one full decode step (28 layers + LM head) at position 4096."""
+    import synth
+    from oracle.model import OracleModel
+    orc = OracleModel(s, layers, head, kv=kv, capacity=s.kv_prefill + 2)
+    tok = synth.start_token(seed, s.vocab)
+    t0 = time.perf_counter()
+    orc.step_token(tok, s.kv_prefill)
+    dt = time.perf_counter() - t0
+    cores = len(os.sched_getaffinity(0))
+    return {"value": 1.0 / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"one full decode step (28 layers + LM head, pos 4096) of the fp64 numpy oracle: {dt:.2f} s"}
+
+
+def run_reference(args):
+    """Reference arm: the CPU oracle on the same workload; each step = one decoder layer of one
+    token (attention + FFN of layer i mod 28 at position 4096 + i mod 256), throughput scaled
+    by that layer's share of the token's algorithmic bytes."""
+    if int(os.environ.get("RANK", "0")) != 0:
+        return  # the oracle runs once, on rank 0; other ranks exit without work
+    import synth
+    from oracle.model import OracleModel
+    from persistent_megakernel_gb300 import roofline as R
+    s, layers, head, kv = build_workload(args.seed)
+    orc = OracleModel(s, layers, head, kv=kv, capacity=s.kv_prefill + CHAIN + 1, cache_weights=True)
+    x = orc.embed(synth.start_token(args.seed, s.vocab))
+    per_token = R.algorithmic_bytes(s, s.kv_prefill)
+    layer_bytes = R.layer_weight_bytes(s) + R.kv_bytes(s, s.kv_prefill) / s.n_layers
+
+    def one(i):
+        l, pos = i % s.n_layers, s.kv_prefill + (i % CHAIN)
+        y = orc.attention_block(l, x, pos)
+        orc.ffn_block(l, y, {})
+
+    for i in range(args.warmup):
+        one(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        one(args.warmup + i)
+    dt = time.perf_counter() - t0
+    value = args.steps * (layer_bytes / per_token) / dt
+    cores = len(os.sched_getaffinity(0))
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"dense_2b: {s.n_layers} layers, hidden 2560, GQA 20/4 x 128, FFN 6912, vocab 32768, "
+                               "KV prefill 4096, batch 1", "step": "one decoder layer of one token"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": "one decoder layer (attention + FFN) per step, fp64 numpy, weights pre-decoded"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def timed_generate(dec, ctx_handle, tok0, pos0, K, launches_per_step):
+    """K greedy steps in chains of CHAIN on the device; returns (seconds by CUDA events, launches)."""
+    import torch
+    from persistent_megakernel_gb300 import binding as B
+    out = torch.empty(CHAIN, dtype=torch.int32, device=dec.device)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(dec.stream)
+    done, launches = 0, 0
+    while done < K:
+        n = min(CHAIN, K - done)
+        B.dec_generate(ctx_handle, tok0, pos0, n, out)
+        launches += B.dec_last_launch_count(ctx_handle)
+        done += n
+    e1.record(dec.stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e-3, launches
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1024)
+    ap.add_argument("--warmup", type=int, default=16)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--mode", default="persistent", choices=["persistent", "per_op", "graph"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-compare", action="store_true", help="skip the launch-per-op comparison")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="profiling captures only: fewer decoder layers (the line is then not the workload's)")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    if args.impl == "reference":
+        return run_reference(args)
+
+    rank, ws, local = dist_setup(args.gpus)
+    import torch
+    import synth
+    from persistent_megakernel_gb300 import build as pbuild
+    pbuild.build()
+    from persistent_megakernel_gb300 import binding as B
+    from persistent_megakernel_gb300 import roofline as R
+    from persistent_megakernel_gb300.model import Decoder
+
+    dev = f"cuda:{local}"
+    torch.cuda.set_device(local)
+    s, layers, head, kv = build_workload(args.seed, args.layers)
+    cap = s.kv_prefill + CHAIN + 8
+    dec = Decoder(s, layers, head, kv=kv, capacity=cap, mode=args.mode, device=dev)
+    tok0 = synth.start_token(args.seed, s.vocab)
+    pos0 = s.kv_prefill
+
+    # warm-up, then exactly K timed steps bracketed by barrier + synchronize
+    timed_generate(dec, dec.ctx, tok0, pos0, args.warmup, 1)
+    clocks = Clocks(local)
+    clocks.start()
+    barrier(ws)
+    torch.cuda.synchronize()
+    secs, launches = timed_generate(dec, dec.ctx, tok0, pos0, args.steps, 1)
+    torch.cuda.synchronize()
+    barrier(ws)
+    clk = clocks.stop()
+    secs_max = max_over_ranks(secs, ws)
+    value = ws * args.steps / secs_max
+
+    # algorithmic bytes per step averaged over the positions the timed steps used
+    poss = [pos0 + (i % CHAIN) for i in range(args.steps)]
+    bytes_step = float(np.mean([R.algorithmic_bytes(s, p) for p in poss]))
+    launch_s = secs / launches
+    peak, peak_kind = peaks()
+    achieved = bytes_step * (1 if args.mode == "persistent" else 1) / (secs / args.steps) / 1e9
+    traffic = ncu_traffic("megakernel_dense_2b.md", kernel_sources()) if args.mode == "persistent" else None
+
+    # end to end through the C ABI with host buffers: token in, argmax out, every step
+    K2 = min(args.steps, CHAIN)
+    tok = tok0
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(K2):
+        tok = B.dec_step(dec.ctx, tok, None, pos0 + i, None, True)
+    e2e_secs = time.perf_counter() - t0
+    e2e_secs = max_over_ranks(e2e_secs, ws)
+    e2e = {"value": ws * K2 / e2e_secs, "unit": "tokens/s", "h2d_bytes_per_step": 60, "d2h_bytes_per_step": 36,
+           "steps": K2, "note": "dec_step per token: token and position copied in, argmax and status copied out"}
+
+    compare = None
+    if not args.no_compare and args.mode == "persistent":
+        compare = {}
+        Kc = min(args.steps, CHAIN)
+        for mode in ("per_op", "graph"):
+            ctx, wsb = dec.context(mode)
+            timed_generate(dec, ctx, tok0, pos0, 4, 1)
+            t, L = timed_generate(dec, ctx, tok0, pos0, Kc, 1)
+            compare[mode] = {"tokens_s": Kc / t, "launches_per_step": L / Kc, "steps": Kc}
+            B.dec_free(ctx)
+            del wsb
+        compare["persistent"] = {"tokens_s": args.steps / secs, "launches_per_step": launches / args.steps}
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(s, layers, head, kv, args.seed)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * secs_max / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"dense_2b: {s.n_layers} layers, hidden 2560, GQA 20/4 x 128, SwiGLU 6912, vocab 32768, "
+                                   "KV prefill 4096, batch 1, greedy, chains of 256 steps (pos 4096-4351)",
+                       "weights": "bf16 ~N(0,0.02) seeded, accumulate fp32", "mode": args.mode,
+                       "l2": "no flush: each step streams %.2f GB > 129 MB L2" % (bytes_step / 1e9),
+                       "parallelism": f"replicas x{ws}"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_kind": peak_kind, "traffic": traffic,
+                         "algorithmic_bytes_per_launch": bytes_step, "launch_us": launch_s * 1e6,
+                         "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
+                         "kernel": "dec_megakernel (one launch per decode step)"},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches,
+            "clocks": clk,
+            "compare_launch_modes": compare,
+        }
+        print(json.dumps(line))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -56,7 +56,7 @@ typedef enum {
 } dec_dtype;
 
 typedef enum {
-  DEC_MODE_PERSISTENT = 0, /* one cooperative launch per step; ops chained by device counters */
+  DEC_MODE_PERSISTENT = 0, /* one cooperative launch per step; ops chained through tagged data */
   DEC_MODE_PER_OP = 1,     /* the same kernel launched once per op (launch-per-op comparison) */
   DEC_MODE_PER_OP_GRAPH = 2, /* the per-op launches of one step replayed as a CUDA graph */
 } dec_mode;
@@ -151,14 +151,24 @@ dec_status dec_generate(dec_ctx* ctx, int32_t token, int32_t pos, int n, int32_t
 dec_status dec_verify(dec_ctx* ctx, const int32_t* tokens_host, const void* hidden_dev, int k,
                       int32_t pos, float* logits_dev, int32_t* argmax_host, int32_t* n_accepted);
 
-/* Device pointer of the residual stream after every block of the last call: fp32
-   [2 n_layers + 1][max_verify][H] (entry 0 is the input, then after attention and after
-   the FFN of each layer), and of the qkv projections fp32 [n_layers][max_verify][qkv rows].
+/* Device pointers of the activations the last call handed between SMs, as tagged 64-bit
+   words: the fp32 value in the low 32 bits, the step's tag in the high 32 bits. hidden: the
+   residual stream [2 n_layers + 1][max_verify][H] (entry 2l+1 after the attention block of
+   layer l, entry 2l+2 after its FFN; entry 0 is unused, the input comes from the embedding
+   or hidden_dev); qkv: the projections [n_layers][max_verify][qkv rows]; routing: one
+   routing block per MoE layer (n_slots, expert ids, slot weights, per-token top-k).
    For inspection and tests; valid until the next call on the stream. */
-dec_status dec_debug_buffers(dec_ctx* ctx, const float** hidden, const float** qkv,
+dec_status dec_debug_buffers(dec_ctx* ctx, const uint64_t** hidden, const uint64_t** qkv,
                              const int32_t** routing);
 
-/* Clear a sticky device error: resets counters and the status word (stream-ordered). */
+/* Self-timing records of the last call (builds compiled with DEC_TRACE; *records is NULL
+   otherwise): uint64 [n_ctas][n_ops][8] %globaltimer nanoseconds per (CTA, op): consumer op
+   start, input ready, prologue done, all warps' tiles done, op end; producer first issue, last
+   issue, and the count of tiles issued. Zero the region between calls to read one call. */
+dec_status dec_trace_buffer(dec_ctx* ctx, const uint64_t** records, int* n_ctas, int* n_ops);
+
+/* Clear a sticky device error: zeroes the whole workspace (step counters, status word and
+   every handed-over activation) after waiting for the stream. Weights and KV cache are kept. */
 dec_status dec_reset(dec_ctx* ctx);
 
 /* Wait for the context's stream; returns a sticky device error if one was raised. */

@@ -9,7 +9,9 @@ import ctypes
 import os
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "libdec.so")
+# DEC_LIB_VARIANT=trace selects the self-timing build (libdec_trace.so)
+_VARIANT = os.environ.get("DEC_LIB_VARIANT", "")
+LIB_PATH = os.path.join(HERE, f"libdec_{_VARIANT}.so" if _VARIANT else "libdec.so")
 
 DEC_OK = 0
 DEC_ERR_INVALID_ARG = 1
@@ -34,7 +36,7 @@ DEC_MODE_PER_OP_GRAPH = 2
 # every symbol include/dec.h declares
 EXPORTS = ("dec_workspace_bytes", "dec_init", "dec_load_weights", "dec_set_kv_cache", "dec_step", "dec_generate",
            "dec_verify", "dec_debug_buffers", "dec_reset", "dec_sync", "dec_last_launch_count", "dec_last_error",
-           "dec_free", "dec_packed_bytes", "dec_pack", "dec_pack_pair")
+           "dec_free", "dec_packed_bytes", "dec_pack", "dec_pack_pair", "dec_trace_buffer")
 
 
 class DecConfig(ctypes.Structure):
@@ -76,6 +78,7 @@ def lib():
             "dec_generate": (I, [P, ctypes.c_int32, ctypes.c_int32, I, P]),
             "dec_verify": (I, [P, P, P, I, ctypes.c_int32, P, P, P]),
             "dec_debug_buffers": (I, [P, ctypes.POINTER(P), ctypes.POINTER(P), ctypes.POINTER(P)]),
+            "dec_trace_buffer": (I, [P, ctypes.POINTER(P), ctypes.POINTER(I), ctypes.POINTER(I)]),
             "dec_reset": (I, [P]),
             "dec_sync": (I, [P]),
             "dec_last_launch_count": (I, [P]),
@@ -156,6 +159,13 @@ def dec_debug_buffers(ctx: int):
     h, q, r = ctypes.c_void_p(), ctypes.c_void_p(), ctypes.c_void_p()
     check(lib().dec_debug_buffers(ctx, ctypes.byref(h), ctypes.byref(q), ctypes.byref(r)))
     return h.value, q.value, r.value
+
+
+def dec_trace_buffer(ctx: int):
+    """(device pointer or None, n_ctas, n_ops) of the self-timing records."""
+    r, c, o = ctypes.c_void_p(), ctypes.c_int(), ctypes.c_int()
+    check(lib().dec_trace_buffer(ctx, ctypes.byref(r), ctypes.byref(c), ctypes.byref(o)))
+    return r.value, c.value, o.value
 
 
 def dec_reset(ctx: int) -> None:

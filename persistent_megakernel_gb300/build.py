@@ -17,6 +17,12 @@ ROOT = os.path.dirname(HERE)
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libdec.so")
 BUILD_DIR = os.path.join(HERE, "_build")
+# "trace": the self-timing variant (-DDEC_TRACE), a separate library next to the default one
+VARIANTS = {"": [], "trace": ["-DDEC_TRACE"]}
+
+
+def lib_path(variant: str = "") -> str:
+    return LIB if not variant else os.path.join(HERE, f"libdec_{variant}.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -36,31 +42,35 @@ def sources():
     return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB):
+def _stale(lib: str) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     deps = sources() + glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh")) + [
         os.path.join(INCLUDE, "dec.h")]
     return any(os.path.getmtime(p) > t for p in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra_nvcc=()) -> str:
-    if not force and not _stale():
-        return LIB
+def build(force: bool = False, verbose: bool = False, extra_nvcc=(), variant: str = "", defines=()) -> str:
+    """Build libdec.so (or libdec_<variant>.so with the variant's -D flags plus `defines`)."""
+    lib = lib_path(variant)
+    if not force and not _stale(lib):
+        return lib
+    defs = VARIANTS.get(variant, []) + list(defines)
     nvcc = _nvcc()
     cuda = _cuda_home(nvcc)
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    bdir = os.path.join(BUILD_DIR, variant or "default")
+    os.makedirs(bdir, exist_ok=True)
     procs = []
     objs = []
     for src in sources():
-        obj = os.path.join(BUILD_DIR, os.path.basename(src) + ".o")
+        obj = os.path.join(bdir, os.path.basename(src) + ".o")
         objs.append(obj)
         if src.endswith(".cu"):
-            cmd = [nvcc, *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE,
+            cmd = [nvcc, *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, *defs,
                    "-Xptxas", "-v" if verbose else "-O3", *extra_nvcc, "-c", src, "-o", obj]
         else:
-            cmd = ["g++", "-O2", "-std=c++17", "-fPIC", "-fopenmp", "-I", INCLUDE, "-I", os.path.join(cuda, "include"),
+            cmd = ["g++", "-O2", "-std=c++17", "-fPIC", "-fopenmp", "-I", INCLUDE, "-I", os.path.join(cuda, "include"), *defs,
                    "-c", src, "-o", obj]
         procs.append((cmd, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)))
     failed = []
@@ -73,14 +83,15 @@ def build(force: bool = False, verbose: bool = False, extra_nvcc=()) -> str:
     if failed:
         msg = "\n".join(" ".join(c) + "\n" + o for c, o in failed)
         raise RuntimeError("building libdec.so failed:\n" + msg)
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     link = [nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart", "-lgomp"]
     r = subprocess.run(link, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)
     if r.returncode != 0:
         raise RuntimeError("linking libdec.so failed:\n" + r.stdout)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
+                variant="trace" if "--trace" in sys.argv else ""))

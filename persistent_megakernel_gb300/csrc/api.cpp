@@ -17,7 +17,6 @@
 using namespace decimpl;
 
 extern "C" cudaError_t dec_launch_megakernel(const KParams* kp, int cooperative, cudaStream_t stream);
-extern "C" size_t dec_megakernel_smem_bytes(int nslot, int act_bytes);
 extern "C" int dec_megakernel_common_bytes(void);
 
 namespace {
@@ -57,9 +56,9 @@ struct LayerW {
 };
 
 struct Layout {  // byte offsets into the workspace
-  size_t state, status, ctr, tickets, ops, hs, qkv, attn_out, hbuf, rlogits, route, eh, part, logits, am_val, am_idx,
-      am_out, total;
-  int n_ops, n_tickets, n_ctas, ns_max, nslot, act_bytes;
+  size_t state, status, tickets, ops, hs, qkv, attn_out, hbuf, rlogits, route, eh, part, logits, am_val, am_idx,
+      am_out, trace, total;
+  int n_ops, n_tickets, n_ctas, ns_max, slot_bytes, act_bytes, exp_stage_all;
 };
 
 bool validate(const dec_config* c, std::string& why) {
@@ -72,7 +71,8 @@ bool validate(const dec_config* c, std::string& why) {
   if (attn) {
     if (c->head_dim != kHeadDim) return bad("head_dim must be 128");
     if (c->n_kv <= 0 || c->n_q % c->n_kv) return bad("n_q must be a multiple of n_kv");
-    if (c->n_q / c->n_kv > 8) return bad("at most 8 query heads per kv head");
+    const int G = c->n_q / c->n_kv;
+    if (G != 1 && G != 2 && G != 4 && G != 5 && G != 8) return bad("query heads per kv head must be 1, 2, 4, 5 or 8");
     if (c->kv_capacity < 1) return bad("kv_capacity must be positive");
   }
   if (c->ffn < 0 || c->ffn % 8) return bad("ffn must be a multiple of 8");
@@ -122,23 +122,35 @@ int pow2_floor(int v) {
 
 int gcd(int a, int b) { return b ? gcd(b, a % b) : a; }
 
-// Tile geometry of a [N][K] matrix of dtype wt: threads per row group and rows per tile.
-void tile_geometry(int wt, int K, int pair, int& tpr, int& rpt, int& unit) {
-  const int cw = wt == W_BF16 ? 8 : (wt == W_FP8 ? 16 : 32);
-  const int nv = K / cw;
-  tpr = std::min(kConsumerThreads, std::max(32, pow2_floor(nv)));
-  const int rows_max = (kConsumerThreads / tpr) * kRmax;
-  const int rb = wt == W_BF16 ? 2 * K : (wt == W_FP8 ? K : K / 2);
-  const int sb = wt == W_MXFP4 ? K / 32 : 0;
+// Tile geometry of a [N][K] matrix of dtype wt streamed through `slot`-byte warp slots:
+// rows per tile R (nr * M <= 32 results per warp), columns per tile Kc, and the row
+// granularity `unit` of the CTA / warp split (gate/up pairs; 16-byte MXFP4 scale copies).
+void tile_geometry(int wt, int K, int pair, int slot, int Mmax, int& R, int& Kc, int& unit) {
+  const double bpc = wt == W_BF16 ? 2.0 : (wt == W_FP8 ? 1.0 : 0.5 + 1.0 / 32.0);
   unit = pair ? 2 : 1;
   if (wt == W_MXFP4) {
-    const int us = 16 / gcd(16, sb);
+    const int us = 16 / gcd(16, K / 32);
     unit = unit * us / gcd(unit, us);
   }
-  int r = std::min(rows_max, kSlotBytes / (rb + sb));
-  while (r > 0 && (((size_t)r * rb + 15) / 16 * 16 + (size_t)r * sb > (size_t)kSlotBytes)) --r;
-  r = r / unit * unit;
-  rpt = r;
+  const int rmax = std::min(kRmax, 32 / Mmax) / unit * unit;
+  auto fits = [&](int r, int kc) {
+    const size_t vb = wt == W_BF16 ? (size_t)2 * kc : (wt == W_FP8 ? (size_t)kc : (size_t)kc / 2);
+    const size_t sb = wt == W_MXFP4 ? (size_t)kc / 32 : 0;
+    return ((size_t)r * vb + 15) / 16 * 16 + (size_t)r * sb <= (size_t)slot;
+  };
+  if (fits(unit, K)) {
+    int r = rmax;
+    while (r > unit && !fits(r, K)) r -= unit;
+    R = r;
+    Kc = K;
+    return;
+  }
+  // a row does not fit: split the columns; two rows per tile share each activation load
+  R = std::max(unit, std::min(2, rmax));
+  const int gran = wt == W_BF16 ? 256 : 512;
+  int kc = (int)((double)slot / (R * bpc)) / gran * gran;
+  while (kc > gran && !fits(R, kc)) kc -= gran;
+  Kc = kc;
 }
 
 bool compute_layout(const dec_config* c, Layout& L, std::string& why) {
@@ -153,31 +165,45 @@ bool compute_layout(const dec_config* c, Layout& L, std::string& why) {
   L.n_ctas = C;
   L.n_ops = count_ops(c);
   L.ns_max = c->n_q ? std::max(1, C / c->n_kv) : 1;
-  L.n_tickets = (c->n_q ? nl * c->n_kv : 0) + (c->n_experts ? nl : 0) + 1 + 1;
+  L.n_tickets = 2;  // LM-head argmax, step end
 
-  // shared-memory scratch ("act") the largest op needs
-  size_t act = (size_t)M * H * 4;
-  act = std::max(act, (size_t)2 * kConsumerThreads * 4);
+  // shared-memory scratch ("act") the largest op needs, in floats
+  const int rows_cta = (H + C - 1) / C + 16;
+  size_t act = (size_t)M * H;
+  act = std::max(act, (size_t)2 * kConsumerThreads);
   if (c->n_q) {
     const size_t MG = (size_t)M * G;
-    act = std::max(act, (size_t)M * c->n_q * kHeadDim * 4);
-    act = std::max(act, (MG * 128 + MG * 64 + 96 + 2 * kMmax * 256 / 4 + 16 * 128 + MG * L.ns_max) * 4);
+    act = std::max(act, (size_t)M * c->n_q * kHeadDim + (size_t)rows_cta * M * (1 + kConsumerWarps));
+    // queries, per-warp scores (<= 32 rows) reused for the merge products, per-warp merge state,
+    // own keys/values, merge weights
+    const size_t prods = ((MG * 32 + L.ns_max - 1) / L.ns_max + 1) * L.ns_max * 4;
+    act = std::max(act, MG * 128 + std::max((size_t)kConsumerWarps * G * 32, prods) + 4 +
+                            (size_t)kConsumerWarps * G * kPart + 2 * kMmax * 128 / 2 + MG * L.ns_max + 64);
   }
-  if (c->ffn) act = std::max(act, (size_t)M * c->ffn * 4);
+  if (c->ffn) act = std::max(act, (size_t)M * c->ffn + (size_t)rows_cta * M * (1 + kConsumerWarps));
+  act = std::max(act, (size_t)M * H + (size_t)2 * (rows_cta + 1) * M * kConsumerWarps);  // column-split partials
+  L.exp_stage_all = 0;
   if (c->n_experts) {
-    act = std::max(act, (size_t)M * c->n_experts * 4);
-    const int rows_cta = (H + C - 1) / C + 16;
-    act = std::max(act, ((size_t)kMmax * c->moe_inter + (size_t)rows_cta * M) * 4);
+    act = std::max(act, (size_t)M * c->n_experts);
+    const size_t per_slot = (size_t)M * c->moe_inter + 2 * (size_t)rows_cta * M;
+    const size_t all = (size_t)(c->n_shared + c->top_k * M) * M * c->moe_inter + 2 * (size_t)rows_cta * M;
+    if (all <= std::max(act, (size_t)7168)) {
+      act = std::max(act, all);
+      L.exp_stage_all = 1;
+    } else {
+      act = std::max(act, per_slot);
+    }
   }
-  act = align_up(act, 16);
+  act = align_up(act * 4, 256);
   const int common = dec_megakernel_common_bytes();
   const long long room = (long long)kSmemLimit - (long long)act - common;
-  const int nslot = (int)std::min<long long>(kMaxSlots, room / kSlotBytes);
-  if (nslot < 2) {
+  long long slot = room / (kConsumerWarps * kStages) / 256 * 256;
+  slot = std::min<long long>(slot, kMaxSlotBytes);
+  if (slot < 4096) {
     why = "shapes need more shared memory than a CTA has";
     return false;
   }
-  L.nslot = nslot;
+  L.slot_bytes = (int)slot;
   L.act_bytes = (int)act;
 
   size_t o = 0;
@@ -188,21 +214,27 @@ bool compute_layout(const dec_config* c, Layout& L, std::string& why) {
   };
   L.state = take(sizeof(StepState));
   L.status = take(sizeof(Status));
-  L.ctr = take((size_t)std::max(1, L.n_ops) * 4);
   L.tickets = take((size_t)L.n_tickets * 4);
   L.ops = take((size_t)std::max(1, L.n_ops) * sizeof(OpDesc));
-  L.hs = take((size_t)(2 * nl + 1) * M * H * 4);
-  L.qkv = take((size_t)nl * M * qkv_rows * 4);
-  L.attn_out = take((size_t)nl * M * c->n_q * kHeadDim * 4);
-  L.hbuf = take((size_t)nl * M * c->ffn * 4);
-  L.rlogits = take((size_t)nl * M * c->n_experts * 4);
+  // activations handed between CTAs are tagged 8-byte words (see ptx.cuh), one buffer per
+  // layer so that no word is written twice in a step
+  L.hs = take((size_t)(2 * nl + 1) * M * H * 8);
+  L.qkv = take((size_t)nl * M * qkv_rows * 8);
+  L.attn_out = take((size_t)nl * M * c->n_q * kHeadDim * 8);
+  L.hbuf = take((size_t)nl * M * c->ffn * 8);
+  L.rlogits = take((size_t)nl * M * c->n_experts * 8);
   L.route = take((size_t)(c->n_experts ? nl : 0) * sizeof(RouteBlock));
-  L.eh = take((size_t)(c->n_experts ? nl : 0) * kMaxRouteSlots * M * c->moe_inter * 4);
-  L.part = take((size_t)(c->n_q ? c->n_kv : 0) * L.ns_max * M * G * 130 * 4);
+  L.eh = take((size_t)(c->n_experts ? nl : 0) * kMaxRouteSlots * M * c->moe_inter * 8);
+  L.part = take((size_t)(c->n_q ? nl * c->n_kv : 0) * L.ns_max * M * G * kPart * 8);
   L.logits = take((size_t)M * c->vocab * 4);
   L.am_val = take((size_t)C * kMmax * 4);
   L.am_idx = take((size_t)C * kMmax * 4);
   L.am_out = take((size_t)kMmax * 4);
+#ifdef DEC_TRACE
+  L.trace = take((size_t)C * std::max(1, L.n_ops) * kTraceFields * 8 + (size_t)kConsumerWarps * kTileLog * kTileStamps * 8);
+#else
+  L.trace = 0;
+#endif
   L.total = o;
   return true;
 }
@@ -259,27 +291,42 @@ void build_ops(dec_ctx* c) {
   const Layout& L = c->lay;
   const int C = L.n_ctas, M = g.max_verify, H = g.hidden;
   const int qkv_rows = g.n_q ? (g.n_q + 2 * g.n_kv) * kHeadDim : 0;
-  float* hs = wsp<float>(c, L.hs);
+  uint64_t* hs = wsp<uint64_t>(c, L.hs);
   std::vector<OpDesc>& ops = c->ops;
   ops.clear();
   int ticket = 0;
   // x of the next block: the call's input first, then the hidden-stream entry last written
   int xsrc = g.embedding ? X_EMBED : X_HIDDEN_IN, x_idx = 0;
-  int prev = -1;  // op whose completion (all CTAs) makes x ready
   auto blank = [&](int type) {
     OpDesc o;
     std::memset(&o, 0, sizeof(o));
     o.type = type;
-    o.wait_ctr = o.wait2_ctr = o.pwait_ctr = -1;
-    o.sig_ctr = (int)ops.size();
     o.xsrc = xsrc;
     o.x_idx = x_idx;
     o.x_src = c->embed;
     o.slot1 = -1;
     return o;
   };
-  auto geom = [&](OpDesc& o) { tile_geometry(o.wtype, o.K, o.pair, o.tpr, o.rpt, o.unit); };
-  auto hs_at = [&](int idx) { return hs + (size_t)idx * M * H; };
+  auto geom = [&](OpDesc& o) {
+    tile_geometry(o.wtype, o.K, o.pair, L.slot_bytes, M, o.R, o.Kc, o.unit);
+    // rows too wide for one slot (or for activations in registers): split the columns across
+    // the CTA's warps instead of its rows (bf16 / FP8 matrices without expert slots)
+    const int cw = o.wtype == W_BF16 ? 8 : (o.wtype == W_FP8 ? 16 : 32);
+    const int ni = o.wtype == W_BF16 ? 10 : (o.wtype == W_FP8 ? 5 : 3);
+    const bool experts = o.type == OP_SHARED_GATEUP || o.type == OP_ROUTED_GATEUP || o.type == OP_EXP_DOWN;
+    if (!experts && o.type != OP_LMHEAD && o.wtype != W_MXFP4 && (o.Kc < o.K || o.K > 32 * ni * cw)) {
+      const int kw = ((o.K + kConsumerWarps - 1) / kConsumerWarps + cw - 1) / cw * cw;
+      const int bpc = o.wtype == W_BF16 ? 2 : 1;
+      int r = std::min(kRmax, 32 / M);
+      while (r > o.unit && (size_t)r * kw * bpc > (size_t)L.slot_bytes) r -= o.unit;
+      if ((size_t)r * kw * bpc <= (size_t)L.slot_bytes && kw <= 32 * ni * cw) {
+        o.csplit = 1;
+        o.Kc = kw;
+        o.R = r / o.unit * o.unit;
+      }
+    }
+  };
+  auto hs_at = [&](int idx) { return hs + (size_t)idx * M * H; };  // tagged [Mmax][H]
 
   for (int l = 0; l < g.n_layers; ++l) {
     const LayerW& w = c->layers[l];
@@ -292,23 +339,16 @@ void build_ops(dec_ctx* c) {
       q.norm = 1;
       q.gain = static_cast<const uint16_t*>(w.attn_norm);
       q.w = w.wqkv;
-      q.out = wsp<float>(c, L.qkv) + (size_t)l * M * qkv_rows;
-      if (prev >= 0) { q.wait_ctr = prev; q.wait_n = C; }
+      q.out = wsp<uint64_t>(c, L.qkv) + (size_t)l * M * qkv_rows;
       geom(q);
-      const int qi = (int)ops.size();
       ops.push_back(q);
 
       OpDesc a = blank(OP_ATTN);
       a.layer = l;
-      a.wait_ctr = qi;
-      a.wait_n = C;
       a.act = q.out;
-      a.out = wsp<float>(c, L.attn_out) + (size_t)l * M * g.n_q * kHeadDim;
+      a.out = wsp<uint64_t>(c, L.attn_out) + (size_t)l * M * g.n_q * kHeadDim;
       a.kc = c->kc + (size_t)l * g.n_kv * g.kv_capacity * kHeadDim;
       a.vc = c->vc + (size_t)l * g.n_kv * g.kv_capacity * kHeadDim;
-      a.ticket = ticket;
-      ticket += g.n_kv;
-      const int ai = (int)ops.size();
       ops.push_back(a);
 
       OpDesc o = blank(OP_OPROJ);
@@ -319,10 +359,7 @@ void build_ops(dec_ctx* c) {
       o.w = w.wo;
       o.act = a.out;
       o.x_out = hs_at(2 * l + 1);
-      o.wait_ctr = ai;
-      o.wait_n = g.n_kv;
       geom(o);
-      prev = (int)ops.size();
       ops.push_back(o);
       xsrc = X_F32;
       x_idx = 2 * l + 1;
@@ -337,10 +374,8 @@ void build_ops(dec_ctx* c) {
       u.norm = 1;
       u.gain = static_cast<const uint16_t*>(w.ffn_norm);
       u.w = w.wgateup;
-      u.out = wsp<float>(c, L.hbuf) + (size_t)l * M * g.ffn;
-      if (prev >= 0) { u.wait_ctr = prev; u.wait_n = C; }
+      u.out = wsp<uint64_t>(c, L.hbuf) + (size_t)l * M * g.ffn;
       geom(u);
-      const int ui = (int)ops.size();
       ops.push_back(u);
 
       OpDesc d = blank(OP_DOWN);
@@ -351,10 +386,7 @@ void build_ops(dec_ctx* c) {
       d.w = w.wdown;
       d.act = u.out;
       d.x_out = hs_at(2 * l + 2);
-      d.wait_ctr = ui;
-      d.wait_n = C;
       geom(d);
-      prev = (int)ops.size();
       ops.push_back(d);
       xsrc = X_F32;
       x_idx = 2 * l + 2;
@@ -362,7 +394,8 @@ void build_ops(dec_ctx* c) {
     if (g.n_experts) {
       const int I = g.moe_inter, E = g.n_experts;
       int32_t* route = reinterpret_cast<int32_t*>(wsp<uint8_t>(c, L.route) + (size_t)l * sizeof(RouteBlock));
-      float* eh = wsp<float>(c, L.eh) + (size_t)l * kMaxRouteSlots * M * I;
+      uint64_t* eh = wsp<uint64_t>(c, L.eh) + (size_t)l * kMaxRouteSlots * M * I;
+      uint64_t* rlogits = wsp<uint64_t>(c, L.rlogits) + (size_t)l * M * E;
       const int64_t gu_v = (int64_t)2 * I * (H / 2), gu_s = (int64_t)2 * I * (H / 32);
       const int64_t dn_v = (int64_t)H * (I / 2), dn_s = (int64_t)H * (I / 32);
 
@@ -374,15 +407,12 @@ void build_ops(dec_ctx* c) {
       r.norm = 1;
       r.gain = static_cast<const uint16_t*>(w.ffn_norm);
       r.w = w.wrouter;
-      r.out = wsp<float>(c, L.rlogits) + (size_t)l * M * E;
+      r.out = rlogits;
+      r.act = rlogits;  // routing ops read the layer's router logits
       r.route = route;
-      r.ticket = ticket++;
-      if (prev >= 0) { r.wait_ctr = prev; r.wait_n = C; }
       geom(r);
-      const int ri = (int)ops.size();
       ops.push_back(r);
 
-      int si = -1;
       if (g.n_shared) {
         OpDesc sg = blank(OP_SHARED_GATEUP);
         sg.layer = l;
@@ -400,9 +430,7 @@ void build_ops(dec_ctx* c) {
         sg.slot1 = g.n_shared;
         sg.eh = eh;
         sg.route = route;
-        if (prev >= 0) { sg.wait_ctr = prev; sg.wait_n = C; }
         geom(sg);
-        si = (int)ops.size();
         ops.push_back(sg);
       }
       OpDesc rg = blank(OP_ROUTED_GATEUP);
@@ -421,12 +449,8 @@ void build_ops(dec_ctx* c) {
       rg.slot1 = -1;
       rg.eh = eh;
       rg.route = route;
-      rg.wait_ctr = ri;
-      rg.wait_n = 1;
-      rg.pwait_ctr = ri;
-      rg.pwait_n = 1;
+      rg.act = rlogits;
       geom(rg);
-      const int rgi = (int)ops.size();
       ops.push_back(rg);
 
       OpDesc dn = blank(OP_EXP_DOWN);
@@ -440,14 +464,10 @@ void build_ops(dec_ctx* c) {
       dn.ws_mstride = dn_s;
       dn.eh = eh;
       dn.route = route;
+      dn.act = rlogits;
       dn.x_out = hs_at(2 * l + 2);
-      dn.wait_ctr = rgi;
-      dn.wait_n = C;
-      if (si >= 0) { dn.wait2_ctr = si; dn.wait2_n = C; }
-      dn.pwait_ctr = ri;
-      dn.pwait_n = 1;
+      dn.stage_all = L.exp_stage_all;
       geom(dn);
-      prev = (int)ops.size();
       ops.push_back(dn);
       xsrc = X_F32;
       x_idx = 2 * l + 2;
@@ -462,10 +482,8 @@ void build_ops(dec_ctx* c) {
     h.gain = static_cast<const uint16_t*>(c->final_norm);
     h.w = c->lm_v;
     h.ws = c->lm_s;
-    h.out = wsp<float>(c, L.logits);
+    h.logits = wsp<float>(c, L.logits);
     h.ticket = ticket++;
-    h.sig_ctr = -1;
-    if (prev >= 0) { h.wait_ctr = prev; h.wait_n = C; }
     geom(h);
     ops.push_back(h);
   }
@@ -494,18 +512,20 @@ void build_ops(dec_ctx* c) {
   k.eps = g.rms_eps;
   k.rope_base = g.rope_base;
   k.timeout_ns = g.spin_timeout_ns ? g.spin_timeout_ns : 2000000000ull;
-  k.nslot = L.nslot;
+  k.slot_bytes = L.slot_bytes;
   k.act_bytes = L.act_bytes;
   k.state = wsp<StepState>(c, L.state);
   k.status = wsp<Status>(c, L.status);
-  k.ctr = wsp<uint32_t>(c, L.ctr);
   k.tickets = wsp<uint32_t>(c, L.tickets);
-  k.part = wsp<float>(c, L.part);
+  k.part = wsp<uint64_t>(c, L.part);
   k.am_val = wsp<float>(c, L.am_val);
   k.am_idx = wsp<int32_t>(c, L.am_idx);
   k.am_out = wsp<int32_t>(c, L.am_out);
   k.step_ticket = ticket++;
   k.hs = hs;
+#ifdef DEC_TRACE
+  k.trace = wsp<uint64_t>(c, L.trace);
+#endif
 }
 
 dec_status prepare(dec_ctx* c) {
@@ -818,20 +838,34 @@ dec_status dec_generate(dec_ctx* c, int32_t token, int32_t pos, int n, int32_t* 
   return DEC_OK;
 }
 
-dec_status dec_debug_buffers(dec_ctx* c, const float** hidden, const float** qkv, const int32_t** routing) {
+dec_status dec_debug_buffers(dec_ctx* c, const uint64_t** hidden, const uint64_t** qkv, const int32_t** routing) {
   if (!c) return fail(DEC_ERR_INVALID_ARG, "null context");
-  if (hidden) *hidden = wsp<float>(c, c->lay.hs);
-  if (qkv) *qkv = wsp<float>(c, c->lay.qkv);
+  if (hidden) *hidden = wsp<uint64_t>(c, c->lay.hs);
+  if (qkv) *qkv = wsp<uint64_t>(c, c->lay.qkv);
   if (routing) *routing = reinterpret_cast<const int32_t*>(c->ws + c->lay.route);
+  return DEC_OK;
+}
+
+dec_status dec_trace_buffer(dec_ctx* c, const uint64_t** records, int* n_ctas, int* n_ops) {
+  if (!c) return fail(DEC_ERR_INVALID_ARG, "null context");
+#ifdef DEC_TRACE
+  if (records) *records = wsp<uint64_t>(c, c->lay.trace);
+#else
+  if (records) *records = nullptr;
+#endif
+  if (n_ctas) *n_ctas = c->lay.n_ctas;
+  if (n_ops) *n_ops = c->lay.n_ops;
   return DEC_OK;
 }
 
 dec_status dec_reset(dec_ctx* c) {
   if (!c) return fail(DEC_ERR_INVALID_ARG, "null context");
-  // counters, tickets, status and the device-owned epoch restart from zero
+  // the whole workspace restarts from zero: tickets, status, the device-owned epoch, and every
+  // tagged activation (their tags restart with the epoch, so no stale word may survive)
   CUDA_TRY(cudaStreamSynchronize(c->stream));
-  CUDA_TRY(cudaMemsetAsync(c->ws + c->lay.state, 0, c->lay.ops - c->lay.state, c->stream));
+  CUDA_TRY(cudaMemsetAsync(c->ws, 0, c->lay.total, c->stream));
   CUDA_TRY(cudaStreamSynchronize(c->stream));
+  c->ops_dirty = true;  // the op list lives in the workspace too
   c->sticky = false;
   c->sticky_code = DEC_OK;
   return DEC_OK;

@@ -2,29 +2,35 @@
 //
 // A decode step is a fixed list of ops (OpDesc). Every CTA of the persistent grid walks
 // the whole list; for each op it takes its own share of the op's rows (or attention
-// positions), split into tiles that fit one shared-memory ring slot. A producer warp
-// streams tiles of weights / KV history into the ring with bulk asynchronous copies;
-// eight consumer warps wait on the op's input (a global counter), compute, and signal the
-// op's own counter. Weights and cached KV never depend on the running step, so the
-// producer runs ahead of the consumers across op boundaries: the next op's weights are
+// positions) and splits it among its consumer warps, in tiles that fit one ring slot. The
+// producer warp streams every consumer warp's tiles of weights / KV history into that
+// warp's slots with bulk asynchronous copies. Weights and cached KV never depend on the
+// running step, so the producer runs ahead across op boundaries: the next op's weights are
 // already in flight while the previous op is still being finished elsewhere (the
 // multiprogramming argument of the Muse Spark Open megakernel article, section "the
 // baseline nobody benchmarked", and its weight-prefetch ring, section "three bills").
+// Activations travel as tagged words (value + step tag): a consumer polls the data it needs
+// instead of a counter, so no writer ever executes a fence.
 #pragma once
 #include <stdint.h>
 
 namespace decimpl {
 
-constexpr int kConsumerWarps = 8;
+// 7 consumer warps + 1 producer warp: two warps per scheduler, so a thread may hold up to 255
+// registers (a ninth warp would put three on one scheduler and cap every thread at 168).
+constexpr int kConsumerWarps = 7;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
-constexpr int kSlotBytes = 32768;                // one ring slot
-constexpr int kMaxSlots = 8;                     // ring slots at most
-constexpr int kRmax = 8;                         // rows one thread accumulates per tile
+constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp (lane w serves consumer warp w)
+#ifndef DEC_STAGES
+#define DEC_STAGES 2
+#endif
+constexpr int kStages = DEC_STAGES;              // ring slots per consumer warp
+constexpr int kRmax = 8;                         // rows one warp accumulates per tile
 constexpr int kMmax = 4;                         // tokens per call (verify window)
 constexpr int kHeadDim = 128;
-constexpr int kAttnTilePos = 64;                 // positions per attention tile: 64 x 256 B x (K+V) = 32 KB
 constexpr int kMaxRouteSlots = 1 + 8 * kMmax;    // shared + union of routed experts
+constexpr int kPart = 132;                       // attention partial: max, sum, 2 pad, output[128]
+constexpr int kMaxSlotBytes = 16384;             // one warp's ring slot at most (attention rows <= 32)
 constexpr int kSmemLimit = 232448;               // dynamic shared memory per CTA on sm_103a
 
 enum OpType : int32_t {
@@ -33,7 +39,7 @@ enum OpType : int32_t {
   OP_OPROJ = 2,         // x' = x + W_o o
   OP_GATEUP = 3,        // b = RMSNorm(x'); h = silu(W_g b) * (W_u b)   (pair-interleaved rows)
   OP_DOWN = 4,          // x'' = x' + W_d h
-  OP_ROUTER = 5,        // b = RMSNorm(x'); r = W_r b (fp32); top-k + softmax (last CTA)
+  OP_ROUTER = 5,        // b = RMSNorm(x'); r = W_r b (fp32); top-k + softmax (every CTA, locally)
   OP_SHARED_GATEUP = 6, // h_s = SwiGLU gate/up of the shared experts (MXFP4)
   OP_ROUTED_GATEUP = 7, // h_e = SwiGLU gate/up of the routed experts (MXFP4)
   OP_EXP_DOWN = 8,      // x'' = x' + sum_slots w * W_d,e h_e
@@ -45,26 +51,27 @@ enum XSrc : int32_t { X_NONE = 0, X_F32 = 1, X_HIDDEN_IN = 2, X_EMBED = 3 };
 
 struct OpDesc {
   int32_t type, wtype, layer, N;      // N: rows of one matrix (per expert for expert ops)
-  int32_t K, rpt, tpr, pair;          // cols, rows per tile, threads per row group, pair rows
-  int32_t wait_ctr, wait_n;           // consumer dependency: counter, contributions per step
-  int32_t wait2_ctr, wait2_n;         // second dependency (-1: none)
-  int32_t pwait_ctr, pwait_n;         // producer dependency (routing), -1: none
-  int32_t sig_ctr, ticket;            // counter this op signals; ticket base (attention, router, head)
+  int32_t K, R, Kc, pair;             // cols, rows per tile, columns per tile, gate/up pair rows
+  int32_t ticket, pad0;               // ticket index (LM head argmax)
   int32_t norm, xsrc;                 // input = RMSNorm(x) * gain; source of x
   int32_t slot0, slot1;               // expert slots [slot0, slot1) (slot1 < 0: up to n_slots)
   int32_t x_idx, unit;                // hidden-stream entry of x (X_F32); row granularity of the CTA split
+  int32_t stage_all, csplit;          // expert down: all hidden vectors staged; column split across warps
   const void* w;                      // packed values (expert ops: expert 0)
   const void* ws;                     // scales plane (FP8 row scales / MXFP4 E8M0), else null
   int64_t w_mstride, ws_mstride;      // bytes between experts
   const uint16_t* gain;               // RMSNorm gain, bf16 [H]
   const void* x_src;                  // X_EMBED: embedding table bf16 [V][H]
-  float* x_out;                       // residual output fp32 [Mmax][H]
-  const float* act;                   // plain input fp32 [Mmax][K] (o-proj: attention out; down: h)
-  float* out;                         // output fp32: qkv [Mmax][qkv], h [Mmax][F], router logits, LM logits
+  uint64_t* x_out;                    // residual output, tagged [Mmax][H]
+  const uint64_t* act;                // plain input, tagged [Mmax][K] (o-proj: attention out; down: h;
+                                      // attention: this layer's qkv)
+  uint64_t* out;                      // output, tagged: qkv [Mmax][qkv], h [Mmax][F], router logits,
+                                      // attention out [Mmax][n_q 128]
+  float* logits;                      // LM head: fp32 logits [Mmax][V] (plain, for the caller)
   uint16_t* kc;                       // this layer's key cache  bf16 [n_kv][cap][128]
   uint16_t* vc;                       // this layer's value cache bf16 [n_kv][cap][128]
   int32_t* route;                     // this layer's RouteBlock
-  float* eh;                          // this layer's expert hidden fp32 [slots][Mmax][I]
+  uint64_t* eh;                       // this layer's expert hidden, tagged [slots][Mmax][I]
 };
 
 struct RouteBlock {
@@ -100,17 +107,27 @@ struct KParams {
   int32_t H, n_q, n_kv, G, qkv_rows, E, top_k, I, n_shared, V, cap, Mmax, L, ns_max;
   float eps, rope_base;
   uint64_t timeout_ns;
-  int32_t nslot, act_bytes;
+  int32_t slot_bytes, act_bytes;      // bytes of one warp's ring slot; shared-memory scratch
   StepState* state;
   Status* status;
-  uint32_t* ctr;
   uint32_t* tickets;
-  float* part;                        // attention partials [n_kv][ns_max][Mmax*G][2 + 128]
+  uint64_t* part;                     // attention partials, tagged [n_kv][ns_max][Mmax*G][kPart]
   float* am_val;                      // argmax partials [n_ctas][Mmax]
   int32_t* am_idx;
   int32_t* am_out;                    // argmax [Mmax]
   int32_t step_ticket;                // ticket index of the step-end rendezvous
-  float* hs;                          // hidden stream fp32 [2L + 1][Mmax][H]
+  uint64_t* hs;                       // hidden stream, tagged [2L + 1][Mmax][H]
+  uint64_t* trace;                    // DEC_TRACE builds: [n_ctas][n_ops][kTraceFields] %globaltimer stamps
 };
+
+// Trace record of one (CTA, op), DEC_TRACE builds only (compiled out otherwise):
+// consumer op start, input ready, prologue done, all warps' tiles done, op end;
+// producer first issue, last issue, tiles issued.
+constexpr int kTraceFields = 8;
+// DEC_TRACE builds also log the first kTileLog tiles of every consumer warp of CTA 0, in SM
+// clock cycles (clock64): issued by the producer, consumer starts waiting, data landed,
+// compute done, slot released (5 stamps + pad per tile).
+constexpr int kTileLog = 1024;
+constexpr int kTileStamps = 6;
 
 }  // namespace decimpl

@@ -3,6 +3,8 @@
 #pragma once
 #include <stdint.h>
 
+#include "dec_internal.h"
+
 namespace decimpl {
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -34,6 +36,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
+}
+
+// Non-blocking probe of a phase's completion.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Generic-proxy accesses to shared memory before this point are ordered before async-proxy
+// (bulk copy) accesses after it.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // Global -> shared bulk copy completing `bytes` transactions on mbarrier `bar`.
@@ -77,19 +96,65 @@ __device__ __forceinline__ uint64_t gtimer() {
   return t;
 }
 
-// Barrier of the 256 consumer threads only (the producer warp never joins).
-__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+// Barrier of the consumer threads only (the producer warp never joins).
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
+}
 
-// Barrier of the 256 consumers that also ANDs a predicate over them: every thread gets the
-// same verdict, so no consumer can leave a loop that the others stay in.
+// Barrier of the consumers that also ANDs a predicate over them: every thread gets the same
+// verdict, so no consumer can leave a loop that the others stay in.
 __device__ __forceinline__ bool consumer_all(bool ok) {
   uint32_t r;
   asm volatile(
-      "{ .reg .pred p, q; setp.ne.u32 p, %1, 0; bar.red.and.pred q, 1, 256, p; selp.u32 %0, 1, 0, q; }"
+      "{ .reg .pred p, q; setp.ne.u32 p, %1, 0; bar.red.and.pred q, 1, %2, p; selp.u32 %0, 1, 0, q; }"
       : "=r"(r)
-      : "r"((uint32_t)ok)
+      : "r"((uint32_t)ok), "n"(kConsumerThreads)
       : "memory");
   return r != 0u;
+}
+
+// Data-carrying flags: an activation element is a 64-bit word, the fp32 value in the low half
+// and the tag of the step that wrote it in the high half, stored with one relaxed 8-byte store
+// (single-copy atomic). A reader polls the data itself until the tag is the current step's:
+// no fence on the writer's side, no counter round trip on the reader's (the sentinel-in-data
+// idea of the Muse Spark Open megakernel article, section "three bills").
+__device__ __forceinline__ uint64_t tagged(float v, uint32_t tag) {
+  return ((uint64_t)tag << 32) | (uint64_t)__float_as_uint(v);
+}
+
+__device__ __forceinline__ void st_tagged(uint64_t* p, float v, uint32_t tag) {
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(tagged(v, tag)) : "memory");
+}
+
+__device__ __forceinline__ void st_tagged4(uint64_t* p, float4 v, uint32_t tag) {  // p 32-byte aligned
+  asm volatile("st.relaxed.gpu.global.v2.b64 [%0], {%1, %2};" ::"l"(p), "l"(tagged(v.x, tag)), "l"(tagged(v.y, tag))
+               : "memory");
+  asm volatile("st.relaxed.gpu.global.v2.b64 [%0], {%1, %2};" ::"l"(p + 2), "l"(tagged(v.z, tag)), "l"(tagged(v.w, tag))
+               : "memory");
+}
+
+__device__ __forceinline__ void ld_tagged2(const uint64_t* p, uint64_t& a, uint64_t& b) {
+  asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+}
+
+__device__ __forceinline__ uint64_t ld_tagged(const uint64_t* p) {
+  uint64_t a;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(a) : "l"(p) : "memory");
+  return a;
+}
+
+__device__ __forceinline__ uint32_t tag_of(uint64_t w) { return (uint32_t)(w >> 32); }
+__device__ __forceinline__ float value_of(uint64_t w) { return __uint_as_float((uint32_t)w); }
+
+// Two fp32 fused multiply-adds in one instruction: (a.x*b.x + c.x, a.y*b.y + c.y), each rounded
+// as fmaf would.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;"
+      : "=l"(d)
+      : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)),
+        "l"(*reinterpret_cast<uint64_t*>(&c)));
+  return *reinterpret_cast<float2*>(&d);
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }

@@ -140,6 +140,7 @@ class Decoder:
             else:
                 reg(B.DEC_T_LM_HEAD, 0, B.DEC_BF16, s.vocab, H, head["w_lm"])
         B.dec_load_weights(self.ctx, tensors)
+        self._tensors = tensors
 
         if s.attn:
             self.k_cache = torch.zeros((s.n_layers, s.n_kv, self.capacity, s.head_dim), dtype=torch.int16,
@@ -153,6 +154,20 @@ class Decoder:
             B.dec_set_kv_cache(self.ctx, self.k_cache, self.v_cache)
         torch.cuda.synchronize(self.device)
         self.logits = torch.empty((max_verify, max(s.vocab, 1)), dtype=torch.float32, device=self.device)
+
+    def context(self, mode: str):
+        """Another context over the same packed weights and KV cache (e.g. another launch mode).
+        Returns (ctx, workspace); the caller frees ctx with binding.dec_free."""
+        cfg = make_config(self.shape, self.capacity, self.max_verify, mode, self.cfg.num_ctas, self.cfg.spin_timeout_ns)
+        nbytes = B.dec_workspace_bytes(cfg)
+        ws_all = torch.zeros(nbytes + 256, dtype=torch.uint8, device=self.device)
+        off = (-ws_all.data_ptr()) % 256
+        torch.cuda.synchronize(self.device)
+        ctx = B.dec_init(cfg, self.stream.cuda_stream, ws_all[off:off + nbytes])
+        B.dec_load_weights(ctx, self._tensors)
+        if self.shape.attn:
+            B.dec_set_kv_cache(ctx, self.k_cache, self.v_cache)
+        return ctx, ws_all
 
     def _pack_experts(self, experts, l):
         s = self.shape
@@ -199,12 +214,14 @@ class Decoder:
         return B.dec_last_launch_count(self.ctx)
 
     def hidden_stream(self) -> torch.Tensor:
-        """fp32 [2L + 1, max_verify, H] view of the residual stream of the last call."""
+        """fp32 [2L + 1, max_verify, H] copy of the residual stream of the last call (the low
+        halves of its tagged words)."""
         h, _, _ = B.dec_debug_buffers(self.ctx)
         s = self.shape
         n = (2 * s.n_layers + 1) * self.max_verify * s.hidden
         off = h - self.ws.data_ptr()
-        return self.ws[off:off + 4 * n].view(torch.float32).view(2 * s.n_layers + 1, self.max_verify, s.hidden)
+        words = self.ws[off:off + 8 * n].view(torch.float32).view(n, 2)
+        return words[:, 0].contiguous().view(2 * s.n_layers + 1, self.max_verify, s.hidden)
 
     def routing(self, layer: int) -> dict:
         """Routing block of a MoE layer after the last call (slots, per-token top-k)."""
