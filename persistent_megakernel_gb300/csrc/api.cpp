@@ -56,7 +56,7 @@ struct LayerW {
 };
 
 struct Layout {  // byte offsets into the workspace
-  size_t state, status, tickets, ops, hs, qkv, attn_out, hbuf, rlogits, route, eh, part, logits, am_val, am_idx,
+  size_t state, status, tickets, ctr, ops, hs, qkv, attn_out, hbuf, rlogits, route, eh, part, logits, am_val, am_idx,
       am_out, trace, total;
   int n_ops, n_tickets, n_ctas, ns_max, slot_bytes, act_bytes, exp_stage_all;
 };
@@ -174,11 +174,12 @@ bool compute_layout(const dec_config* c, Layout& L, std::string& why) {
   if (c->n_q) {
     const size_t MG = (size_t)M * G;
     act = std::max(act, (size_t)M * c->n_q * kHeadDim + (size_t)rows_cta * M * (1 + kConsumerWarps));
-    // queries, per-warp scores (<= 32 rows) reused for the merge products, per-warp merge state,
-    // own keys/values, merge weights
+    // queries, per-warp scores (<= 32 rows) reused for the merge's output slices, per-warp merge
+    // state, own keys/values, merge weights, the splits' (max, sum), the polled q/k/v rows
     const size_t prods = ((MG * 32 + L.ns_max - 1) / L.ns_max + 1) * L.ns_max * 4;
     act = std::max(act, MG * 128 + std::max((size_t)kConsumerWarps * G * 32, prods) + 4 +
-                            (size_t)kConsumerWarps * G * kPart + 2 * kMmax * 128 / 2 + MG * L.ns_max + 64);
+                            (size_t)kConsumerWarps * G * kPart + 2 * kMmax * 128 / 2 + MG * L.ns_max + 4 +
+                            2 * MG * L.ns_max + (size_t)M * (G + 2) * 128 + 64);
   }
   if (c->ffn) act = std::max(act, (size_t)M * c->ffn + (size_t)rows_cta * M * (1 + kConsumerWarps));
   act = std::max(act, (size_t)M * H + (size_t)2 * (rows_cta + 1) * M * kConsumerWarps);  // column-split partials
@@ -215,6 +216,7 @@ bool compute_layout(const dec_config* c, Layout& L, std::string& why) {
   L.state = take(sizeof(StepState));
   L.status = take(sizeof(Status));
   L.tickets = take((size_t)L.n_tickets * 4);
+  L.ctr = take((size_t)(std::max(1, L.n_ops) + (c->n_q ? nl * c->n_kv : 0)) * 4);
   L.ops = take((size_t)std::max(1, L.n_ops) * sizeof(OpDesc));
   // activations handed between CTAs are tagged 8-byte words (see ptx.cuh), one buffer per
   // layer so that no word is written twice in a step
@@ -297,10 +299,18 @@ void build_ops(dec_ctx* c) {
   int ticket = 0;
   // x of the next block: the call's input first, then the hidden-stream entry last written
   int xsrc = g.embedding ? X_EMBED : X_HIDDEN_IN, x_idx = 0;
+  // every op announces its completion on its own counter; an op waits for the counter of the op
+  // that produced its newest input (ops run in list order in every CTA, so older inputs are
+  // complete too)
+  int prev = -1;
   auto blank = [&](int type) {
     OpDesc o;
     std::memset(&o, 0, sizeof(o));
     o.type = type;
+    o.ctr = (int)ops.size();
+    o.wait_ctr = prev;
+    o.wait_n = C;
+    o.aux_ctr = -1;
     o.xsrc = xsrc;
     o.x_idx = x_idx;
     o.x_src = c->embed;
@@ -342,14 +352,17 @@ void build_ops(dec_ctx* c) {
       q.out = wsp<uint64_t>(c, L.qkv) + (size_t)l * M * qkv_rows;
       geom(q);
       ops.push_back(q);
+      prev = q.ctr;
 
       OpDesc a = blank(OP_ATTN);
       a.layer = l;
       a.act = q.out;
       a.out = wsp<uint64_t>(c, L.attn_out) + (size_t)l * M * g.n_q * kHeadDim;
+      a.aux_ctr = L.n_ops + l * g.n_kv;  // per-kv-head counters of the splits' partials
       a.kc = c->kc + (size_t)l * g.n_kv * g.kv_capacity * kHeadDim;
       a.vc = c->vc + (size_t)l * g.n_kv * g.kv_capacity * kHeadDim;
       ops.push_back(a);
+      prev = a.ctr;
 
       OpDesc o = blank(OP_OPROJ);
       o.layer = l;
@@ -361,6 +374,7 @@ void build_ops(dec_ctx* c) {
       o.x_out = hs_at(2 * l + 1);
       geom(o);
       ops.push_back(o);
+      prev = o.ctr;
       xsrc = X_F32;
       x_idx = 2 * l + 1;
     }
@@ -377,6 +391,7 @@ void build_ops(dec_ctx* c) {
       u.out = wsp<uint64_t>(c, L.hbuf) + (size_t)l * M * g.ffn;
       geom(u);
       ops.push_back(u);
+      prev = u.ctr;
 
       OpDesc d = blank(OP_DOWN);
       d.layer = l;
@@ -388,6 +403,7 @@ void build_ops(dec_ctx* c) {
       d.x_out = hs_at(2 * l + 2);
       geom(d);
       ops.push_back(d);
+      prev = d.ctr;
       xsrc = X_F32;
       x_idx = 2 * l + 2;
     }
@@ -410,8 +426,10 @@ void build_ops(dec_ctx* c) {
       r.out = rlogits;
       r.act = rlogits;  // routing ops read the layer's router logits
       r.route = route;
+      r.aux_ctr = r.ctr;  // the routing waits for every CTA's logits
       geom(r);
       ops.push_back(r);
+      const int x_ready = r.wait_ctr;  // the shared experts read x' like the router
 
       if (g.n_shared) {
         OpDesc sg = blank(OP_SHARED_GATEUP);
@@ -430,6 +448,7 @@ void build_ops(dec_ctx* c) {
         sg.slot1 = g.n_shared;
         sg.eh = eh;
         sg.route = route;
+        sg.wait_ctr = x_ready;
         geom(sg);
         ops.push_back(sg);
       }
@@ -450,6 +469,8 @@ void build_ops(dec_ctx* c) {
       rg.eh = eh;
       rg.route = route;
       rg.act = rlogits;
+      rg.wait_ctr = x_ready;  // its own input is x'; its routing waits for the router (aux)
+      rg.aux_ctr = r.ctr;
       geom(rg);
       ops.push_back(rg);
 
@@ -465,10 +486,13 @@ void build_ops(dec_ctx* c) {
       dn.eh = eh;
       dn.route = route;
       dn.act = rlogits;
+      dn.wait_ctr = rg.ctr;  // routed (and, earlier in every CTA, shared) expert hidden vectors
+      dn.aux_ctr = r.ctr;
       dn.x_out = hs_at(2 * l + 2);
       dn.stage_all = L.exp_stage_all;
       geom(dn);
       ops.push_back(dn);
+      prev = dn.ctr;
       xsrc = X_F32;
       x_idx = 2 * l + 2;
     }
@@ -517,6 +541,7 @@ void build_ops(dec_ctx* c) {
   k.state = wsp<StepState>(c, L.state);
   k.status = wsp<Status>(c, L.status);
   k.tickets = wsp<uint32_t>(c, L.tickets);
+  k.ctr = wsp<uint32_t>(c, L.ctr);
   k.part = wsp<uint64_t>(c, L.part);
   k.am_val = wsp<float>(c, L.am_val);
   k.am_idx = wsp<int32_t>(c, L.am_idx);

@@ -9,8 +9,10 @@
 // already in flight while the previous op is still being finished elsewhere (the
 // multiprogramming argument of the Muse Spark Open megakernel article, section "the
 // baseline nobody benchmarked", and its weight-prefetch ring, section "three bills").
-// Activations travel as tagged words (value + step tag): a consumer polls the data it needs
-// instead of a counter, so no writer ever executes a fence.
+// Activations travel as tagged words (value + step tag). When a CTA has written its share of
+// an op it bumps the op's arrival counter with a relaxed atomic (no fence: a fence would wait
+// for the CTA's bulk copies in flight); a consumer waits for the count with one thread, then
+// loads the data and checks every word's tag, re-reading the rare word not yet visible.
 #pragma once
 #include <stdint.h>
 
@@ -52,7 +54,9 @@ enum XSrc : int32_t { X_NONE = 0, X_F32 = 1, X_HIDDEN_IN = 2, X_EMBED = 3 };
 struct OpDesc {
   int32_t type, wtype, layer, N;      // N: rows of one matrix (per expert for expert ops)
   int32_t K, R, Kc, pair;             // cols, rows per tile, columns per tile, gate/up pair rows
-  int32_t ticket, pad0;               // ticket index (LM head argmax)
+  int32_t ticket, ctr;                // ticket index (LM head argmax); this op's arrival counter
+  int32_t wait_ctr, wait_n;           // counter of the op producing this op's input, arrivals / step
+  int32_t aux_ctr, pad0;              // attention: first per-kv-head counter; routed ops: router's
   int32_t norm, xsrc;                 // input = RMSNorm(x) * gain; source of x
   int32_t slot0, slot1;               // expert slots [slot0, slot1) (slot1 < 0: up to n_slots)
   int32_t x_idx, unit;                // hidden-stream entry of x (X_F32); row granularity of the CTA split
@@ -83,7 +87,8 @@ struct RouteBlock {
 };
 
 struct StepState {
-  uint32_t epoch;                     // completed steps; counters reach (epoch+1)*n during a step
+  uint32_t epoch;                     // completed steps; counters reach (epoch+1)*n during a step;
+                                      // activation tags are epoch + 1
   int32_t pos;                        // position of the first token of this call
   int32_t m;                          // tokens in this call (1..kMmax)
   int32_t chain;                      // 1: at step end feed argmax back as the next token, pos += 1
@@ -111,6 +116,7 @@ struct KParams {
   StepState* state;
   Status* status;
   uint32_t* tickets;
+  uint32_t* ctr;                      // arrival counters: one per op, then one per (layer, kv head)
   uint64_t* part;                     // attention partials, tagged [n_kv][ns_max][Mmax*G][kPart]
   float* am_val;                      // argmax partials [n_ctas][Mmax]
   int32_t* am_idx;
@@ -122,8 +128,9 @@ struct KParams {
 
 // Trace record of one (CTA, op), DEC_TRACE builds only (compiled out otherwise):
 // consumer op start, input ready, prologue done, all warps' tiles done, op end;
-// producer first issue, last issue, tiles issued.
-constexpr int kTraceFields = 8;
+// producer first issue, last issue, tiles issued; first thread's input loads done, input words
+// found not yet visible (re-polled), attention merge start, attention merge inputs ready.
+constexpr int kTraceFields = 12;
 // DEC_TRACE builds also log the first kTileLog tiles of every consumer warp of CTA 0, in SM
 // clock cycles (clock64): issued by the producer, consumer starts waiting, data landed,
 // compute done, slot released (5 stamps + pad per tile).

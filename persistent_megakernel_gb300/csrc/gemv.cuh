@@ -81,23 +81,25 @@ __device__ __forceinline__ void warp_gemv(const uint8_t* slot, int nr, int kn, i
           const uint32_t ww[4] = {w[u][j].x, w[u][j].y, w[u][j].z, w[u][j].w};
 #pragma unroll
           for (int m = 0; m < MT; ++m) {
-            float2 c0 = A.c[j][m][0], c1 = A.c[j][m][1];
+            // one token: two chains per row; several tokens: their chains are already independent
+            float2 c0 = A.c[j][m][0], c1 = MT == 1 ? A.c[j][m][1] : make_float2(0.f, 0.f);
+            float2& cb = *(MT == 1 ? &c1 : &c0);
             if constexpr (WT == W_BF16) {
               // word e holds weights 2e, 2e+1; quarter q = e / 2 holds activations 4q .. 4q+3
               c0 = ffma2(make_float2(bf16_lo(ww[0]), bf16_hi(ww[0])), make_float2(a[u][m][0].x, a[u][m][0].y), c0);
-              c1 = ffma2(make_float2(bf16_lo(ww[1]), bf16_hi(ww[1])), make_float2(a[u][m][0].z, a[u][m][0].w), c1);
+              cb = ffma2(make_float2(bf16_lo(ww[1]), bf16_hi(ww[1])), make_float2(a[u][m][0].z, a[u][m][0].w), cb);
               c0 = ffma2(make_float2(bf16_lo(ww[2]), bf16_hi(ww[2])), make_float2(a[u][m][1].x, a[u][m][1].y), c0);
-              c1 = ffma2(make_float2(bf16_lo(ww[3]), bf16_hi(ww[3])), make_float2(a[u][m][1].z, a[u][m][1].w), c1);
+              cb = ffma2(make_float2(bf16_lo(ww[3]), bf16_hi(ww[3])), make_float2(a[u][m][1].z, a[u][m][1].w), cb);
             } else {
               // word q holds e4m3 weights 4q .. 4q+3
 #pragma unroll
               for (int q = 0; q < 4; ++q) {
                 c0 = ffma2(e4m3x2_to_float2(ww[q] & 0xFFFFu), make_float2(a[u][m][q].x, a[u][m][q].y), c0);
-                c1 = ffma2(e4m3x2_to_float2(ww[q] >> 16), make_float2(a[u][m][q].z, a[u][m][q].w), c1);
+                cb = ffma2(e4m3x2_to_float2(ww[q] >> 16), make_float2(a[u][m][q].z, a[u][m][q].w), cb);
               }
             }
             A.c[j][m][0] = c0;
-            A.c[j][m][1] = c1;
+            if constexpr (MT == 1) A.c[j][m][1] = c1;
           }
         }
     } else {
@@ -207,67 +209,101 @@ __device__ __forceinline__ void act_regs_load(ActRegs<WT, NI>& R, const float* a
   }
 }
 
+// Pin the accumulators: every FMA feeding them is issued before this point and no memory
+// access moves across it. Bounds how far the compiler may run weight loads ahead of the math.
+template <int NR, int MT>
+__device__ __forceinline__ void acc_pin(Acc<NR, MT>& A) {
+#pragma unroll
+  for (int j = 0; j < NR; ++j)
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+      asm volatile("" : "+f"(A.c[j][m][0].x), "+f"(A.c[j][m][0].y), "+f"(A.c[j][m][1].x), "+f"(A.c[j][m][1].y)::"memory");
+}
+
 // A += W[tile] * act for a tile whose columns are exactly the ones loaded in R (kn = cn).
+// Software-pipelined over groups of F chunks: the loads of group g + 1 are issued before the
+// math of group g, and the accumulators are pinned after it, so at most 2 F NR 16-byte weight
+// vectors are live next to the activations.
 template <int WT, int NR, int NI>
 __device__ __forceinline__ void warp_gemv_reg(const uint8_t* slot, int nr, int kn, const ActRegs<WT, NI>& R,
                                               Acc<NR, 1>& A, int lane) {
   constexpr int CW = WCfg<WT>::CW;
+  constexpr int F = NR >= 8 ? 1 : (NR >= 4 ? 2 : 4);  // chunks per group
+  constexpr int NG = (NI + F - 1) / F;
   const int rb = WT == W_BF16 ? 2 * kn : (WT == W_FP8 ? kn : kn / 2);
   const int NV = kn / CW;
   const uint8_t* scales = slot + ((nr * rb + 15) & ~15);
+  uint4 w[2][F][NR];
+  auto load = [&](int g) {
 #pragma unroll
-  for (int i = 0; i < NI; ++i) {
-    // at most four chunks' weights in flight: bounds the live registers next to the activations
-    if (i % 4 == 0 && i > 0) asm volatile("" ::: "memory");
-    const int v = lane + 32 * i;
-    const bool ok = v < NV;  // chunks past the tile's columns contribute zero (activations are zero there)
-    uint4 w[NR];
+    for (int f = 0; f < F; ++f) {
+      const int i = g * F + f;
+      const int v = lane + 32 * i;
+      // chunks past the tile's columns contribute zero (their activations are zero)
+      const bool ok = i < NI && v < NV;
 #pragma unroll
-    for (int j = 0; j < NR; ++j)
-      w[j] = (ok && j < nr) ? *reinterpret_cast<const uint4*>(slot + (size_t)j * rb + v * 16) : make_uint4(0u, 0u, 0u, 0u);
-    if constexpr (WT == W_BF16) {
+      for (int j = 0; j < NR; ++j)
+        w[g & 1][f][j] = (ok && j < nr) ? *reinterpret_cast<const uint4*>(slot + (size_t)j * rb + v * 16)
+                                        : make_uint4(0u, 0u, 0u, 0u);
+    }
+  };
+  load(0);
 #pragma unroll
-      for (int j = 0; j < NR; ++j) {
-        float2 c0 = A.c[j][0][0], c1 = A.c[j][0][1];
-        c0 = ffma2(make_float2(bf16_lo(w[j].x), bf16_hi(w[j].x)), make_float2(R.a[i][0].x, R.a[i][0].y), c0);
-        c1 = ffma2(make_float2(bf16_lo(w[j].y), bf16_hi(w[j].y)), make_float2(R.a[i][0].z, R.a[i][0].w), c1);
-        c0 = ffma2(make_float2(bf16_lo(w[j].z), bf16_hi(w[j].z)), make_float2(R.a[i][1].x, R.a[i][1].y), c0);
-        c1 = ffma2(make_float2(bf16_lo(w[j].w), bf16_hi(w[j].w)), make_float2(R.a[i][1].z, R.a[i][1].w), c1);
-        A.c[j][0][0] = c0;
-        A.c[j][0][1] = c1;
-      }
-    } else if constexpr (WT == W_FP8) {
+  for (int g = 0; g < NG; ++g) {
+    if (g + 1 < NG) load(g + 1);
 #pragma unroll
-      for (int j = 0; j < NR; ++j) {
-        const uint32_t ww[4] = {w[j].x, w[j].y, w[j].z, w[j].w};
-        float2 c0 = A.c[j][0][0], c1 = A.c[j][0][1];
+    for (int f = 0; f < F; ++f) {
+      const int i = g * F + f;
+      if (i >= NI) break;
+      const uint4* wg = w[g & 1][f];
+      if constexpr (WT == W_BF16) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          c0 = ffma2(e4m3x2_to_float2(ww[q] & 0xFFFFu), make_float2(R.a[i][q].x, R.a[i][q].y), c0);
-          c1 = ffma2(e4m3x2_to_float2(ww[q] >> 16), make_float2(R.a[i][q].z, R.a[i][q].w), c1);
+        for (int j = 0; j < NR; ++j) {
+          float2 c0 = A.c[j][0][0], c1 = A.c[j][0][1];
+          c0 = ffma2(make_float2(bf16_lo(wg[j].x), bf16_hi(wg[j].x)), make_float2(R.a[i][0].x, R.a[i][0].y), c0);
+          c1 = ffma2(make_float2(bf16_lo(wg[j].y), bf16_hi(wg[j].y)), make_float2(R.a[i][0].z, R.a[i][0].w), c1);
+          c0 = ffma2(make_float2(bf16_lo(wg[j].z), bf16_hi(wg[j].z)), make_float2(R.a[i][1].x, R.a[i][1].y), c0);
+          c1 = ffma2(make_float2(bf16_lo(wg[j].w), bf16_hi(wg[j].w)), make_float2(R.a[i][1].z, R.a[i][1].w), c1);
+          A.c[j][0][0] = c0;
+          A.c[j][0][1] = c1;
         }
-        A.c[j][0][0] = c0;
-        A.c[j][0][1] = c1;
-      }
-    } else {
+      } else if constexpr (WT == W_FP8) {
 #pragma unroll
-      for (int j = 0; j < NR; ++j) {
-        const uint32_t ww[4] = {w[j].x, w[j].y, w[j].z, w[j].w};
-        float2 b0 = make_float2(0.f, 0.f), b1 = make_float2(0.f, 0.f);
+        for (int j = 0; j < NR; ++j) {
+          const uint32_t ww[4] = {wg[j].x, wg[j].y, wg[j].z, wg[j].w};
+          float2 c0 = A.c[j][0][0], c1 = A.c[j][0][1];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          // word q: bytes -> weights 8q .. 8q+7, activations quarters 2q, 2q+1
-          b0 = ffma2(e2m1x2_to_float2(ww[q] & 0xFFu), make_float2(R.a[i][2 * q].x, R.a[i][2 * q].y), b0);
-          b1 = ffma2(e2m1x2_to_float2((ww[q] >> 8) & 0xFFu), make_float2(R.a[i][2 * q].z, R.a[i][2 * q].w), b1);
-          b0 = ffma2(e2m1x2_to_float2((ww[q] >> 16) & 0xFFu), make_float2(R.a[i][2 * q + 1].x, R.a[i][2 * q + 1].y), b0);
-          b1 = ffma2(e2m1x2_to_float2(ww[q] >> 24), make_float2(R.a[i][2 * q + 1].z, R.a[i][2 * q + 1].w), b1);
+          for (int q = 0; q < 4; ++q) {
+            c0 = ffma2(e4m3x2_to_float2(ww[q] & 0xFFFFu), make_float2(R.a[i][q].x, R.a[i][q].y), c0);
+            c1 = ffma2(e4m3x2_to_float2(ww[q] >> 16), make_float2(R.a[i][q].z, R.a[i][q].w), c1);
+          }
+          A.c[j][0][0] = c0;
+          A.c[j][0][1] = c1;
         }
-        const float X = (ok && j < nr) ? e8m0_to_float(scales[(size_t)j * (kn / 32) + v]) : 0.f;
-        const float2 xx = make_float2(X, X);
-        A.c[j][0][0] = ffma2(xx, b0, A.c[j][0][0]);
-        A.c[j][0][1] = ffma2(xx, b1, A.c[j][0][1]);
+      } else {
+        const int v = lane + 32 * i;
+        const bool ok = v < NV;
+#pragma unroll
+        for (int j = 0; j < NR; ++j) {
+          const uint32_t ww[4] = {wg[j].x, wg[j].y, wg[j].z, wg[j].w};
+          float2 b0 = make_float2(0.f, 0.f), b1 = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            // word q: bytes -> weights 8q .. 8q+7, activations quarters 2q, 2q+1
+            b0 = ffma2(e2m1x2_to_float2(ww[q] & 0xFFu), make_float2(R.a[i][2 * q].x, R.a[i][2 * q].y), b0);
+            b1 = ffma2(e2m1x2_to_float2((ww[q] >> 8) & 0xFFu), make_float2(R.a[i][2 * q].z, R.a[i][2 * q].w), b1);
+            b0 = ffma2(e2m1x2_to_float2((ww[q] >> 16) & 0xFFu), make_float2(R.a[i][2 * q + 1].x, R.a[i][2 * q + 1].y),
+                       b0);
+            b1 = ffma2(e2m1x2_to_float2(ww[q] >> 24), make_float2(R.a[i][2 * q + 1].z, R.a[i][2 * q + 1].w), b1);
+          }
+          const float X = (ok && j < nr) ? e8m0_to_float(scales[(size_t)j * (kn / 32) + v]) : 0.f;
+          const float2 xx = make_float2(X, X);
+          A.c[j][0][0] = ffma2(xx, b0, A.c[j][0][0]);
+          A.c[j][0][1] = ffma2(xx, b1, A.c[j][0][1]);
+        }
       }
     }
+    acc_pin(A);
   }
 }
 

@@ -44,12 +44,14 @@ namespace decimpl {
 // ------------------------------------------------------------------ shared memory map
 constexpr int kCommonBytes = 9728;
 constexpr int kOffFull = 0, kOffEmpty = 256, kOffOp = 512, kOffRed = 1024, kOffResW = 3072, kOffRope = 5120,
-              kOffFlags = 7168, kOffRoute = 7232;
+              kOffFlags = 7168, kOffRoute = 7232, kOffNTiles = 8192;
 constexpr int kFlagTicket = 1;  // flags[kFlagTicket]: verdict of the last ticket
+constexpr int kFlagLate = 2;    // flags[kFlagLate]: input words re-polled in this op (DEC_TRACE)
 constexpr int kFlagRoute = 8;   // flags[kFlagRoute]: layer + 1 whose routing sits in `route`
 static_assert(kConsumerWarps * kStages * 8 <= kOffEmpty - kOffFull, "full barriers");
 static_assert(sizeof(OpDesc) <= kOffRed - kOffOp, "OpDesc copy");
-static_assert(kOffRoute + sizeof(RouteBlock) <= kCommonBytes, "common area");
+static_assert(kOffRoute + sizeof(RouteBlock) <= kOffNTiles, "routing block");
+static_assert(kOffNTiles + 4 * kConsumerWarps <= kCommonBytes, "common area");
 
 struct Smem {
   uint8_t* ring;        // [warp][stage][slot_bytes]
@@ -62,6 +64,7 @@ struct Smem {
   float2* rope;         // [kMmax][64] (cos, sin) at pos + m
   volatile int* flags;  // [16]
   RouteBlock* route;    // this CTA's routing of the current MoE layer
+  uint32_t* ntiles;     // [warp] tiles each consumer warp has taken from its ring
   int slot_bytes;
   __device__ __forceinline__ uint8_t* slot(int w, int st) const {
     return ring + ((size_t)w * kStages + st) * slot_bytes;
@@ -82,9 +85,16 @@ __device__ __forceinline__ Smem carve(uint8_t* base, const KParams& p) {
   s.rope = reinterpret_cast<float2*>(c + kOffRope);
   s.flags = reinterpret_cast<volatile int*>(c + kOffFlags);
   s.route = reinterpret_cast<RouteBlock*>(c + kOffRoute);
+  s.ntiles = reinterpret_cast<uint32_t*>(c + kOffNTiles);
   s.slot_bytes = p.slot_bytes;
   return s;
 }
+
+// The dynamic shared memory and the step state every device function of the kernel can reach:
+// out-of-line functions rebuild their context from these, the grid-constant parameters and the
+// thread index, so no per-thread state ever travels through local memory.
+extern __shared__ __align__(1024) uint8_t smem_raw[];
+__shared__ StepState g_st;  // copied in by the kernel's first thread
 
 // ------------------------------------------------------------------ failure handling
 __device__ __forceinline__ bool aborted(const KParams& p) {
@@ -124,54 +134,76 @@ __device__ __forceinline__ bool wait_mbar(const KParams& p, uint32_t bar, uint32
   return wait_mbar_slow(p, bar, parity, op, where);
 }
 
-// Poll n (1 or 4) tagged words at src until all carry `tag`; bounded like every wait.
-__device__ __noinline__ bool poll_slow(const KParams& p, const uint64_t* src, int n, uint32_t tag, float* out,
-                                       int op, uint32_t where) {
+// Spin until the arrival counter reaches target (wrap-safe), bounded like every wait.
+__device__ __noinline__ bool wait_counter_slow(const KParams& p, const uint32_t* c, uint32_t target, int op,
+                                               uint32_t where) {
   const uint64_t t0 = gtimer();
   for (int it = 1;; ++it) {
-    bool all = true;
-    for (int i = 0; i < n; ++i) {
-      const uint64_t w = ld_tagged(src + i);
-      if (tag_of(w) == tag)
-        out[i] = value_of(w);
-      else
-        all = false;
-    }
-    if (all) return true;
-    if ((it & 7) == 0) {
+    const uint32_t v = ld_relaxed(c);
+    if ((int32_t)(v - target) >= 0) return true;
+    if ((it & 15) == 0) {
       if (aborted(p)) return false;
       if (gtimer() - t0 > p.timeout_ns) {
-        raise_error(p, DEC_ERR_TIMEOUT, op, 0x40000000u, tag_of(ld_tagged(src)), tag, where);
+        raise_error(p, DEC_ERR_TIMEOUT, op, (uint32_t)(c - p.ctr), v, target, where);
         return false;
       }
     }
   }
 }
 
-// Four tagged words at src (16-byte aligned).
-__device__ __forceinline__ bool poll4(const KParams& p, const uint64_t* src, uint32_t tag, float4& v, int op,
-                                      uint32_t where) {
-  uint64_t a, b, c, d;
-  ld_tagged2(src, a, b);
-  ld_tagged2(src + 2, c, d);
-  if (tag_of(a) == tag && tag_of(b) == tag && tag_of(c) == tag && tag_of(d) == tag) {
-    v = make_float4(value_of(a), value_of(b), value_of(c), value_of(d));
-    return true;
+#ifndef DEC_STREAM_EVICT_FIRST
+#define DEC_STREAM_EVICT_FIRST 1  // weights / KV history stream through L2 as evict-first
+#endif
+#ifndef DEC_INFLIGHT_KB
+#define DEC_INFLIGHT_KB 256  // bytes of weight / KV copies one SM may keep in flight, in KiB
+#endif
+constexpr int kInflightBytes = DEC_INFLIGHT_KB * 1024;
+#ifndef DEC_ORDERED_ARRIVALS
+#define DEC_ORDERED_ARRIVALS 0  // 1: release/acquire arrivals (data visible when the count is)
+#endif
+#ifndef DEC_POLL_BACKOFF_NS
+#define DEC_POLL_BACKOFF_NS 0  // pause before re-reading words whose tag is not current yet
+#endif
+#ifndef DEC_GATHER_U
+#define DEC_GATHER_U 8  // 4-word items each thread keeps in flight when loading an op's input
+#endif
+constexpr int kGatherU = DEC_GATHER_U;
+
+// One item of W tagged words (W = 2 or 4: 16-byte aligned).
+template <int W>
+__device__ __forceinline__ void ld_item(const uint64_t* s, uint64_t (&w)[W]) {
+  if constexpr (W == 1) {
+    w[0] = ld_tagged(s);
+  } else {
+    ld_tagged2(s, w[0], w[1]);
+    if constexpr (W == 4) ld_tagged2(s + 2, w[2], w[3]);
   }
-  float o[4];
-  const bool ok = poll_slow(p, src, 4, tag, o, op, where);
-  v = make_float4(o[0], o[1], o[2], o[3]);
-  return ok;
 }
 
-__device__ __forceinline__ bool poll1(const KParams& p, const uint64_t* src, uint32_t tag, float& v, int op,
-                                      uint32_t where) {
-  const uint64_t a = ld_tagged(src);
-  if (tag_of(a) == tag) {
-    v = value_of(a);
-    return true;
+// Re-poll one item of W tagged words until every word carries `tag` (values into out), bounded
+// like every wait. Out of line: it runs only for the rare word still in flight after its
+// producers' arrival count was seen.
+template <int W>
+__device__ __noinline__ bool poll_item_slow(const KParams& p, const uint64_t* src, float* out, uint32_t tag, int op,
+                                            uint32_t where) {
+  const uint64_t t0 = gtimer();
+  for (int it = 1;; ++it) {
+    uint64_t w[W];
+    ld_item<W>(src, w);
+    bool good = true;
+    for (int k = 0; k < W; ++k) good &= tag_of(w[k]) == tag;
+    if (good) {
+      for (int k = 0; k < W; ++k) out[k] = value_of(w[k]);
+      return true;
+    }
+    if ((it & 7) == 0) {
+      if (aborted(p)) return false;
+      if (gtimer() - t0 > p.timeout_ns) {
+        raise_error(p, DEC_ERR_TIMEOUT, op, 0x40000000u, tag_of(w[0]), tag, where);
+        return false;
+      }
+    }
   }
-  return poll_slow(p, src, 1, tag, &v, op, where);
 }
 
 // ------------------------------------------------------------------ work partition
@@ -230,7 +262,7 @@ struct GemvIter {
   const int* experts;  // expert id per slot (routed ops); null: expert id = mat_base + slot
   int mat_base;
 
-  __device__ void init(const OpDesc& op, int C, int cta, int w, int n_slots, const int* expert_ids, int base) {
+  __device__ __forceinline__ void init(const OpDesc& op, int C, int cta, int w, int n_slots, const int* expert_ids, int base) {
     mat_base = base;
     N = op.N;
     K = op.K;
@@ -263,7 +295,7 @@ struct GemvIter {
     sl = 0;
   }
 
-  __device__ bool next(Tile& t) {
+  __device__ __forceinline__ bool next(Tile& t) {
     if (mode == 3) {
       if (r >= bw || kw0 >= kw1) return false;
       t.mat = 0;
@@ -321,7 +353,7 @@ struct AttnIter {
   int j, q, qe, head;
   bool fresh;
 
-  __device__ void init(const KParams& p, int cta, int w, int pos_, int M, int P_) {
+  __device__ __forceinline__ void init(const KParams& p, int cta, int w, int pos_, int M, int P_) {
     C = p.n_ctas;
     pos = pos_;
     S = pos + M;
@@ -334,7 +366,7 @@ struct AttnIter {
     fresh = true;
   }
 
-  __device__ void enter_split() {
+  __device__ __forceinline__ void enter_split() {
     int s, p0, p1;
     split_range(S, ns, j, head, s, p0, p1);
     const int ce = max(p0, min(p1, pos));
@@ -344,7 +376,7 @@ struct AttnIter {
   }
 
   // Next tile of the current split only (the consumer steps splits itself).
-  __device__ bool next_in_split(Tile& t) {
+  __device__ __forceinline__ bool next_in_split(Tile& t) {
     if (fresh) enter_split();
     if (q >= qe) return false;
     t.mat = head;
@@ -355,14 +387,14 @@ struct AttnIter {
     return true;
   }
 
-  __device__ bool next_split() {
+  __device__ __forceinline__ bool next_split() {
     j += C;
     fresh = true;
     return j < nsplit;
   }
 
   // Producer: next tile across splits.
-  __device__ bool next(Tile& t) {
+  __device__ __forceinline__ bool next(Tile& t) {
     while (j < nsplit) {
       if (next_in_split(t)) return true;
       next_split();
@@ -389,15 +421,24 @@ struct Producer {
   const KParams& p;
   Smem& s;
   int pos, M;
+  uint64_t policy;  // L2 policy of the streamed bytes
+
+  __device__ __forceinline__ void stream(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+#if DEC_STREAM_EVICT_FIRST
+    bulk_g2s_hint(dst, src, bytes, bar, policy);
+#else
+    bulk_g2s(dst, src, bytes, bar);
+#endif
+  }
 
   // Expert ids of the current MoE layer's routing, once the consumers have published it.
-  __device__ const int* routing(const OpDesc* op) {
+  __device__ __forceinline__ const int* routing(const OpDesc* op) {
     if (s.flags[kFlagRoute] != __ldg(&op->layer) + 1) return nullptr;
     __threadfence_block();
     return s.route->expert;
   }
 
-  __device__ void copy_gemv(const OpDesc* op, const Tile& t, uint8_t* dst, uint32_t fb) {
+  __device__ __forceinline__ void copy_gemv(const OpDesc* op, const Tile& t, uint8_t* dst, uint32_t fb) {
     const int wtype = __ldg(&op->wtype), K = __ldg(&op->K);
     const int rb = row_bytes(wtype, K);
     const char* base = static_cast<const char*>(op->w) + (size_t)t.mat * __ldg(&op->w_mstride);
@@ -408,67 +449,76 @@ struct Producer {
     mbar_expect_tx(fb, total + sbytes);
     const uint32_t d = smem_addr(dst);
     if (t.kn == K) {
-      bulk_g2s(d, base + (size_t)t.r0 * rb, total, fb);
+      stream(d, base + (size_t)t.r0 * rb, total, fb);
     } else {
-      for (int i = 0; i < t.nr; ++i) bulk_g2s(d + i * cb, base + (size_t)(t.r0 + i) * rb + koff, (uint32_t)cb, fb);
+      for (int i = 0; i < t.nr; ++i) stream(d + i * cb, base + (size_t)(t.r0 + i) * rb + koff, (uint32_t)cb, fb);
     }
     if (sbytes) {
       const int K32 = K / 32;
       const char* sb = static_cast<const char*>(op->ws) + (size_t)t.mat * __ldg(&op->ws_mstride);
       const uint32_t d2 = d + ((total + 15u) & ~15u);
       if (t.kn == K) {
-        bulk_g2s(d2, sb + (size_t)t.r0 * K32, sbytes, fb);
+        stream(d2, sb + (size_t)t.r0 * K32, sbytes, fb);
       } else {
         for (int i = 0; i < t.nr; ++i)
-          bulk_g2s(d2 + i * (t.kn / 32), sb + (size_t)(t.r0 + i) * K32 + t.kc / 32, (uint32_t)(t.kn / 32), fb);
+          stream(d2 + i * (t.kn / 32), sb + (size_t)(t.r0 + i) * K32 + t.kc / 32, (uint32_t)(t.kn / 32), fb);
       }
     }
   }
 
-  __device__ void copy_attn(const OpDesc* op, const Tile& t, uint8_t* dst, uint32_t fb) {
+  __device__ __forceinline__ void copy_attn(const OpDesc* op, const Tile& t, uint8_t* dst, uint32_t fb) {
     const uint32_t bytes = (uint32_t)t.nr * 256u;
     const size_t off = ((size_t)t.mat * p.cap + t.r0) * kHeadDim;
     mbar_expect_tx(fb, 2u * bytes);
     const uint32_t d = smem_addr(dst);
-    bulk_g2s(d, op->kc + off, bytes, fb);
-    bulk_g2s(d + bytes, op->vc + off, bytes, fb);
+    stream(d, op->kc + off, bytes, fb);
+    stream(d + bytes, op->vc + off, bytes, fb);
   }
 
-  // One attempt for this lane: returns true if the cursor moved (tile issued or op finished).
-  __device__ bool step(LaneCursor& c, int w) {
-    if (c.oi >= p.op_end) return false;
-    const OpDesc* op = p.ops + c.oi;
-    const int type = __ldg(&op->type);
-    if (!c.started) {
-      if (type == OP_ATTN) {
-        c.a.init(p, blockIdx.x, w, pos, M, s.slot_bytes / 512);
-      } else {
-        const int* experts = nullptr;
-        int n_slots = 0;
-        if (type == OP_ROUTED_GATEUP || type == OP_EXP_DOWN) {
-          experts = routing(op);
-          if (!experts) return false;  // routing not computed yet
-          n_slots = s.route->n_slots;
+  // Bytes a tile brings into its slot.
+  __device__ __forceinline__ uint32_t tile_bytes(const OpDesc* op, int type, const Tile& t) const {
+    if (type == OP_ATTN) return (uint32_t)t.nr * 512u;
+    const int wtype = __ldg(&op->wtype);
+    if (wtype == W_MXFP4) return (uint32_t)(t.nr * (t.kn / 2) + t.nr * (t.kn / 32));
+    return (uint32_t)(t.nr * t.kn * bytes_per_col(wtype));
+  }
+
+  // Point the lane's cursor at its next tile: ops without tiles for this lane are passed over.
+  // Returns false if the lane has no tile to offer right now (all ops done, or a routed op whose
+  // routing is not computed yet).
+  __device__ __forceinline__ bool peek(LaneCursor& c, int w, Tile& t, AttnIter& pa, GemvIter& pg) {
+    while (c.oi < p.op_end) {
+      const OpDesc* op = p.ops + c.oi;
+      const int type = __ldg(&op->type);
+      if (!c.started) {
+        if (type == OP_ATTN) {
+          c.a.init(p, blockIdx.x, w, pos, M, s.slot_bytes / 512);
+        } else {
+          const int* experts = nullptr;
+          int n_slots = 0;
+          if (type == OP_ROUTED_GATEUP || type == OP_EXP_DOWN) {
+            experts = routing(op);
+            if (!experts) return false;  // routing not computed yet
+            n_slots = s.route->n_slots;
+          }
+          c.g.init(*op, p.n_ctas, blockIdx.x, w, n_slots, experts, type == OP_SHARED_GATEUP ? p.E : 0);
         }
-        const OpDesc o = *op;
-        c.g.init(o, p.n_ctas, blockIdx.x, w, n_slots, experts, type == OP_SHARED_GATEUP ? p.E : 0);
+        c.started = 1;
       }
-      c.started = 1;
-    }
-    Tile t;
-    AttnIter pa = c.a;
-    GemvIter pg = c.g;
-    const bool more = type == OP_ATTN ? pa.next(t) : pg.next(t);
-    if (!more) {
+      pa = c.a;
+      pg = c.g;
+      if (type == OP_ATTN ? pa.next(t) : pg.next(t)) return true;
       ++c.oi;
       c.started = 0;
-      return true;
     }
+    return false;
+  }
+
+  __device__ __forceinline__ void issue(LaneCursor& c, int w, const Tile& t, const AttnIter& pa, const GemvIter& pg) {
+    const OpDesc* op = p.ops + c.oi;
     const uint32_t st = c.n % (uint32_t)kStages;
-    const uint32_t parity = ((c.n / (uint32_t)kStages) & 1u) ^ 1u;
-    if (!mbar_test_wait(smem_addr(&s.empty[w * kStages + st]), parity)) return false;
     const uint32_t fb = smem_addr(&s.full[w * kStages + st]);
-    if (type == OP_ATTN) {
+    if (__ldg(&op->type) == OP_ATTN) {
       c.a = pa;
       copy_attn(op, t, s.slot(w, st), fb);
     } else {
@@ -488,10 +538,14 @@ struct Producer {
     }
 #endif
     ++c.n;
-    return true;
   }
 
-  __device__ void run(int lane) {
+  // Lane w streams consumer warp w's tiles. The lanes share one budget of bytes in flight per
+  // SM: a deep queue of weight copies in front of the memory system would make every
+  // latency-critical load of the consumers (activations, counters) wait behind it, while a
+  // budget of about bandwidth x latency keeps HBM just as busy. Each round, one lane whose
+  // warp has a free slot (taken in turn) issues its next tile if the SM is under budget.
+  __device__ __forceinline__ void run(int lane) {
     if (lane >= kConsumerWarps) return;
     constexpr unsigned kMask = (1u << kConsumerWarps) - 1u;
     const int w = lane;
@@ -499,17 +553,55 @@ struct Producer {
     c.oi = p.op_begin;
     c.started = 0;
     c.n = 0;
+    uint32_t bytes[kStages];
+#pragma unroll
+    for (int k = 0; k < kStages; ++k) bytes[k] = 0;
+    int rr = 0;
     uint64_t t_idle = 0;
     for (;;) {
-      const bool moved = step(c, w);
+      Tile t;
+      AttnIter pa;
+      GemvIter pg;
+      const bool have = peek(c, w, t, pa, pg);
       const bool done = c.oi >= p.op_end;
+      const uint32_t st = c.n % (uint32_t)kStages;
+      const bool ready =
+          have && mbar_test_wait(smem_addr(&s.empty[w * kStages + st]), ((c.n / (uint32_t)kStages) & 1u) ^ 1u);
+      // bytes of this lane's copies not landed yet (only the last kStages can be in flight)
+      uint32_t fl = 0;
+#pragma unroll
+      for (int k = 1; k <= kStages; ++k) {
+        if ((uint32_t)k <= c.n) {
+          const uint32_t q = c.n - k;
+          if (!mbar_test_wait(smem_addr(&s.full[w * kStages + q % kStages]), (q / kStages) & 1u))
+            fl += bytes[q % kStages];
+        }
+      }
+      const uint32_t total = __reduce_add_sync(kMask, fl);
+      // ready lanes in turn from lane rr, each while the SM stays under its budget
+      const uint32_t tb = ready ? tile_bytes(p.ops + c.oi, __ldg(&p.ops[c.oi].type), t) : 0u;
+      const int my_turn = (w - rr + kConsumerWarps) % kConsumerWarps;
+      uint32_t before = 0;
+#pragma unroll
+      for (int k = 0; k < kConsumerWarps; ++k) {
+        const uint32_t bk = __shfl_sync(kMask, tb, k);
+        if ((k - rr + kConsumerWarps) % kConsumerWarps < my_turn) before += bk;
+      }
+      const bool grant = ready && total + before < (uint32_t)kInflightBytes;
+      const unsigned granted = __ballot_sync(kMask, grant);
+      if (grant) {
+        bytes[st] = tb;
+        issue(c, w, t, pa, pg);
+      }
+      const bool issued = granted != 0u;
+      if (issued) rr = (rr + 1) % kConsumerWarps;
       if (__all_sync(kMask, done)) break;
-      if (__any_sync(kMask, moved)) {
+      if (issued) {
         t_idle = 0;
         continue;
       }
-      // nothing could move: every live warp's slots are full or routing is pending; back off
-      // so the spinning lanes leave the scheduler's issue slots to the consumers
+      // nothing issued: slots full, budget spent or routing pending; back off so the spinning
+      // lanes leave the scheduler's issue slots to the consumers
       __nanosleep(64);
       int stop = 0;
       if (w == 0) {
@@ -542,27 +634,30 @@ __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 // Scratch in s.act (floats):
 //   q     [M*G][128]         rotated queries of the kv group, times log2(e)/sqrt(128)
 //   sc    [warps][G][P]      scores, then probabilities, of each warp's current tile; reused for
-//                            the merge products
-//   mg    [warps][G][132]    per-warp (max, sum, -, -, output[128]) at the end of a split; reused
-//                            for the splits' sums in the merge
+//                            the splits' output slices in the merge
+//   mg    [warps][G][132]    per-warp (max, sum, -, -, output[128]) at the end of a split
 //   kvn   bf16 [2][M][128]   this call's own keys / values (rotated, rounded)
-//   cw    [M*G][ns]          merge weights
+//   cw    [rows][ns]         merge weights
+//   ml    [ns][rows] float2  the splits' (max, sum) in the merge
+//   raw   [M][G+2][128]      this call's q, k, v rows of the kv group, as polled
 struct AttnScratch {
   float* q;
   float* sc;
   float* mg;
   uint16_t* kvn;
   float* cw;
+  float2* ml;
+  float* raw;
 };
 
 __device__ __forceinline__ AttnScratch attn_scratch(const KParams& p, const Smem& s, int M, int P) {
   AttnScratch a;
+  const int MG = M * p.G, ns = p.ns_max;
   float* f = s.act;
   a.q = f;
-  f += M * p.G * 128;
+  f += MG * 128;
   {
-    const int MG = M * p.G, ns = p.ns_max;
-    const int prods = ((MG * 32 + ns - 1) / ns + 1) * ns * 4;  // merge products (float4) of one slice
+    const int prods = ((MG * 32 + ns - 1) / ns + 1) * ns * 4;  // merge: output slices of every split
     a.sc = f;
     f += max(kConsumerWarps * p.G * P, prods);
     f = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(f) + 15) & ~uintptr_t(15));
@@ -572,6 +667,11 @@ __device__ __forceinline__ AttnScratch attn_scratch(const KParams& p, const Smem
   a.kvn = reinterpret_cast<uint16_t*>(f);
   f += 2 * kMmax * 128 / 2;
   a.cw = f;
+  f += MG * ns;
+  f = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(f) + 15) & ~uintptr_t(15));
+  a.ml = reinterpret_cast<float2*>(f);
+  f += 2 * MG * ns;
+  a.raw = f;
   return a;
 }
 
@@ -666,13 +766,51 @@ __device__ __forceinline__ void attn_warp_tile(AttnState<G_>& A, const float (&q
 }
 
 // ------------------------------------------------------------------ consumer
+struct Consumer;
+template <int WT, int MT, int NR, int NI>
+__device__ __noinline__ bool gemv_tiles_entry(const KParams& p, int oi, const OpDesc& op, int M, float* xres, int a,
+                                              float* accd);
+template <int WT, int MT, int NR, int NI>
+__device__ __noinline__ bool gemv_csplit_entry(const KParams& p, int oi, const OpDesc& op, int M, int a, float* parts);
+template <int MT>
+__device__ __noinline__ bool gemv_slot_entry(const KParams& p, int oi, const OpDesc& op, int sl, int M, int a,
+                                             float* accd);
+__device__ __noinline__ bool gemv_prologue_entry(const KParams& p, int oi, int M);
+__device__ __noinline__ bool gemv_tiles_dispatch_entry(const KParams& p, int oi, int M);
+__device__ __noinline__ bool gemv_epilogue_entry(const KParams& p, int oi, int M);
+__device__ __noinline__ bool routing_entry(const KParams& p, int oi, int M);
+__device__ __noinline__ bool copy_act_entry(const KParams& p, int oi, float* dst, const uint64_t* src, int M, int K,
+                                            int src_stride, int cw);
+template <int G_>
+__device__ __noinline__ bool attn_entry(const KParams& p, int oi, int pos, int M);
+
+// A consumer thread's view of the kernel. Built from scratch wherever it is needed (see
+// smem_raw), so out-of-line functions keep it in registers; the ring position of the thread's
+// warp lives in shared memory between them (save_tiles).
 struct Consumer {
   const KParams& p;
-  Smem& s;
+  Smem s;
   uint32_t epoch, tag;  // tag: the data tag of this step (epoch + 1; zeroed memory never matches)
   const StepState& st;
   int tid, warp, lane;
   uint32_t n_tiles;  // tiles consumed by this warp (ring position)
+
+  __device__ __forceinline__ explicit Consumer(const KParams& p_)
+      : p(p_),
+        s(carve(smem_raw, p_)),
+        epoch(g_st.epoch),
+        tag(g_st.epoch + 1u),
+        st(g_st),
+        tid((int)threadIdx.x),
+        warp((int)threadIdx.x >> 5),
+        lane((int)threadIdx.x & 31),
+        n_tiles(s.ntiles[threadIdx.x >> 5]) {}
+
+  __device__ __forceinline__ void save_tiles() {
+    __syncwarp();
+    if (lane == 0) s.ntiles[warp] = n_tiles;
+    __syncwarp();
+  }
 
 #ifdef DEC_TRACE
   __device__ __forceinline__ void tile_log(int field) {
@@ -694,6 +832,31 @@ struct Consumer {
     }
     consumer_sync();
     return s.flags[kFlagTicket] != 0;
+  }
+
+  // Wait until counter c has n arrivals in this step. One thread spins; the others wait at the
+  // barrier. The data behind the count is then read with its tags checked (gather).
+  __device__ bool wait_counter(int c, int n, int oi, uint32_t where) {
+    bool ok = true;
+    if (tid == 0) {
+      const uint32_t target = (epoch + 1u) * (uint32_t)n;
+      const uint32_t* ctr = p.ctr + c;
+      if ((int32_t)(ld_relaxed(ctr) - target) < 0) ok = wait_counter_slow(p, ctr, target, oi, where);
+#if DEC_ORDERED_ARRIVALS
+      (void)ld_acquire(ctr);
+#endif
+    }
+    return consumer_all(ok);
+  }
+
+  // This CTA has written its share of what counter c announces.
+  __device__ void arrive(int c) {
+    consumer_sync();  // every warp's stores are issued
+#if DEC_ORDERED_ARRIVALS
+    if (tid == 0) red_release(p.ctr + c, 1u);
+#else
+    if (tid == 0) red_relaxed(p.ctr + c, 1u);
+#endif
   }
 
   // Wait for this warp's next tile; the verdict is uniform across the warp.
@@ -718,23 +881,64 @@ struct Consumer {
   }
 
   // ---------------------------------------------------------------- activation loads
+  // Poll n items of W tagged words (item i at addr(i)) and hand each to sink(i, values); every
+  // thread keeps U items in flight, so a prologue whose inputs are ready costs one round trip.
+  template <int U, int W, class Addr, class Sink>
+  __device__ __forceinline__ bool gather(int n, Addr addr, Sink sink, int oi, uint32_t where) {
+    bool ok = true;
+    for (int i0 = tid; i0 < n; i0 += U * kConsumerThreads) {
+      // all U items' loads first, then the checks
+      uint64_t w[U][W];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int i = i0 + u * kConsumerThreads;
+        if (i < n) {
+          ld_item<W>(addr(i), w[u]);
+        } else {
+#pragma unroll
+          for (int k = 0; k < W; ++k) w[u][k] = tagged(0.f, tag);
+        }
+      }
+      uint32_t late = 0;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int i = i0 + u * kConsumerThreads;
+        float v[W];
+        bool good = true;
+#pragma unroll
+        for (int k = 0; k < W; ++k) {
+          v[k] = value_of(w[u][k]);
+          good &= tag_of(w[u][k]) == tag;
+        }
+        if (i < n) {
+          if (good)
+            sink(i, v);
+          else
+            late |= 1u << u;
+        }
+      }
+      // words not yet visible: poll them one by one
+#ifdef DEC_TRACE
+      if (late) atomicAdd(const_cast<int*>(&s.flags[kFlagLate]), __popc(late));
+#endif
+      for (int u = 0; late != 0u; ++u, late >>= 1) {
+        if (!(late & 1u)) continue;
+        const int i = i0 + u * kConsumerThreads;
+        float v[W];
+        if (!poll_item_slow<W>(p, addr(i), v, tag, oi, where)) return false;
+        sink(i, v);
+      }
+    }
+    return ok;
+  }
+
   __device__ __forceinline__ const uint16_t* x_bf16(const OpDesc& op, int m) const {
     return op.xsrc == X_EMBED ? static_cast<const uint16_t*>(op.x_src) + (size_t)st.tokens[m] * p.H
                               : static_cast<const uint16_t*>(st.hidden_in) + (size_t)m * p.H;
   }
 
-  // Four consecutive elements 4*k4 .. +3 of token m's x (the op's residual / norm input).
-  __device__ __forceinline__ bool load_x4(const OpDesc& op, int m, int k4, float4& v, int oi) {
-    if (op.xsrc == X_F32) return poll4(p, p.hs + ((size_t)op.x_idx * p.Mmax + m) * p.H + 4 * k4, tag, v, oi, 7);
-    const uint2 u = __ldg(reinterpret_cast<const uint2*>(x_bf16(op, m)) + k4);
-    v = make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
-    return true;
-  }
-
-  __device__ __forceinline__ bool load_x1(const OpDesc& op, int m, int k, float& v, int oi) {
-    if (op.xsrc == X_F32) return poll1(p, p.hs + ((size_t)op.x_idx * p.Mmax + m) * p.H + k, tag, v, oi, 8);
-    v = __uint_as_float((uint32_t)__ldg(x_bf16(op, m) + k) << 16);
-    return true;
+  __device__ __forceinline__ const uint64_t* x_tagged(const OpDesc& op, int m) const {
+    return p.hs + ((size_t)op.x_idx * p.Mmax + m) * p.H;
   }
 
   // ---------------------------------------------------------------- prologues
@@ -749,96 +953,111 @@ struct Consumer {
     }
   }
 
-  // act = RMSNorm(x_m) * gain (op.norm) or x_m, written in the quarter-plane layout of the op's
-  // weight type; the sum of squares is reduced in a fixed order (lane partials, warp tree,
-  // warps in order), identical in every CTA. Returns this thread's polling verdict.
-  __device__ bool norm_prologue(const OpDesc& op, int M, const uint2 (&gpre)[kGainPre], int oi) {
-    const int H = p.H, H4 = H / 4;
+  // act = RMSNorm(x_m) * gain (op.norm) or x_m for the M tokens, written in the quarter-plane
+  // layout of the op's weight type. Element group i = m*H/4 + k4 belongs to thread i mod
+  // threads in every CTA, so the sum of squares (thread partials in order, warp tree, warps in
+  // order) is the same everywhere. Returns this thread's polling verdict.
+  __device__ __forceinline__ bool norm_prologue(const OpDesc& op, int M, const uint2 (&gpre)[kGainPre], int oi) {
+    const int H = p.H, H4 = H / 4, n4 = M * H4;
     const int cw = chunk_width(op.wtype), nvt = H / cw;
+    auto at = [&](int i) {
+      const int m = i / H4, k4 = i - m * H4;
+      return reinterpret_cast<float4*>(s.act + m * H + act_pos(4 * k4, cw, nvt));
+    };
     bool ok = true;
-    for (int m = 0; m < M; ++m) {
-      float ss = 0.f;
-      for (int i0 = tid; i0 < H4; i0 += 4 * kConsumerThreads) {
-        float4 x[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int i = i0 + u * kConsumerThreads;
-          x[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (i < H4) ok &= load_x4(op, m, i, x[u], oi);
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int i = i0 + u * kConsumerThreads;
-          if (i < H4) *reinterpret_cast<float4*>(s.act + m * H + act_pos(4 * i, cw, nvt)) = x[u];
-          ss = fmaf(x[u].x, x[u].x, ss);
-          ss = fmaf(x[u].y, x[u].y, ss);
-          ss = fmaf(x[u].z, x[u].z, ss);
-          ss = fmaf(x[u].w, x[u].w, ss);
-        }
+    if (op.xsrc == X_F32) {
+      ok = gather<kGatherU, 4>(
+          n4, [&](int i) { return x_tagged(op, i / H4) + 4 * (i % H4); },
+          [&](int i, const float (&v)[4]) { *at(i) = make_float4(v[0], v[1], v[2], v[3]); }, oi, 7);
+      if (tid == 0) TRACE(p, oi, 8, gtimer());
+    } else {
+      for (int i = tid; i < n4; i += kConsumerThreads) {
+        const uint2 u = __ldg(reinterpret_cast<const uint2*>(x_bf16(op, i / H4)) + i % H4);
+        *at(i) = make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
       }
-      if (op.norm) {
+    }
+    if (op.norm) {
+      // every thread sums the squares of the groups it polled itself (token m's groups come in
+      // increasing i), so no barrier is needed before the reduction
+      float ss[kMmax], rstd[kMmax];
+      int i = tid;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-        if (lane == 0) s.red[warp] = ss;
-        consumer_sync();
-        float tot = 0.f;
+      for (int m = 0; m < kMmax; ++m) {
+        float acc = 0.f;
+        if (m < M)
+          for (; i < (m + 1) * H4; i += kConsumerThreads) {
+            const float4 x = *at(i);
+            acc = fmaf(x.x, x.x, acc);
+            acc = fmaf(x.y, x.y, acc);
+            acc = fmaf(x.z, x.z, acc);
+            acc = fmaf(x.w, x.w, acc);
+          }
 #pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) tot += s.red[w];
-        const float rstd = 1.0f / sqrtf(tot / (float)H + p.eps);
-        auto scale = [&](int i, uint2 g) {
-          float4* d = reinterpret_cast<float4*>(s.act + m * H + act_pos(4 * i, cw, nvt));
-          float4 v = *d;
-          v.x = v.x * rstd * bf16_lo(g.x);
-          v.y = v.y * rstd * bf16_hi(g.x);
-          v.z = v.z * rstd * bf16_lo(g.y);
-          v.w = v.w * rstd * bf16_hi(g.y);
-          *d = v;
-        };
-#pragma unroll
-        for (int u = 0; u < kGainPre; ++u) {
-          const int i = tid + u * kConsumerThreads;
-          if (i < H4) scale(i, gpre[u]);
-        }
-        for (int i = tid + kGainPre * kConsumerThreads; i < H4; i += kConsumerThreads)
-          scale(i, __ldg(reinterpret_cast<const uint2*>(op.gain) + i));
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        ss[m] = acc;
+        if (lane == 0) s.red[m * 8 + warp] = acc;
       }
       consumer_sync();
+#pragma unroll
+      for (int m = 0; m < kMmax; ++m) {
+        float tot = 0.f;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) tot += s.red[m * 8 + w];
+        rstd[m] = 1.0f / sqrtf(tot / (float)H + p.eps);
+      }
+      (void)ss;
+      auto scale = [&](int i, uint2 g, float r) {
+        float4* d = at(i);
+        float4 v = *d;
+        v.x = v.x * r * bf16_lo(g.x);
+        v.y = v.y * r * bf16_hi(g.x);
+        v.z = v.z * r * bf16_lo(g.y);
+        v.w = v.w * r * bf16_hi(g.y);
+        *d = v;
+      };
+      if (M == 1) {
+#pragma unroll
+        for (int u = 0; u < kGainPre; ++u) {
+          const int k4 = tid + u * kConsumerThreads;
+          if (k4 < H4) scale(k4, gpre[u], rstd[0]);
+        }
+        for (int k4 = tid + kGainPre * kConsumerThreads; k4 < H4; k4 += kConsumerThreads)
+          scale(k4, __ldg(reinterpret_cast<const uint2*>(op.gain) + k4), rstd[0]);
+      } else {
+        for (int j = tid; j < n4; j += kConsumerThreads) {
+          const int m = j / H4;
+          const float r = m == 0 ? rstd[0] : (m == 1 ? rstd[1] : (m == 2 ? rstd[2] : rstd[3]));
+          scale(j, __ldg(reinterpret_cast<const uint2*>(op.gain) + (j - m * H4)), r);
+        }
+      }
     }
+    consumer_sync();
     return ok;
   }
 
   // dst = M rows of K tagged words polled from global (row stride src_stride words), in the
-  // quarter-plane layout of chunk width cw; four polls in flight per thread.
-  __device__ bool copy_act(float* dst, const uint64_t* src, int M, int K, int src_stride, int cw, int oi) {
-    const int K4 = K / 4, n4 = M * K4, nvt = K / cw;
-    bool ok = true;
-    for (int i0 = tid; i0 < n4; i0 += 4 * kConsumerThreads) {
-      float4 x[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int i = i0 + u * kConsumerThreads;
-        x[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (i < n4) ok &= poll4(p, src + (size_t)(i / K4) * src_stride + 4 * (i % K4), tag, x[u], oi, 9);
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int i = i0 + u * kConsumerThreads;
-        if (i < n4) *reinterpret_cast<float4*>(dst + (i / K4) * K + act_pos(4 * (i % K4), cw, nvt)) = x[u];
-      }
-    }
-    return ok;
+  // quarter-plane layout of chunk width cw.
+  __device__ __forceinline__ bool copy_act(float* dst, const uint64_t* src, int M, int K, int src_stride, int cw, int oi) {
+    const int K4 = K / 4, nvt = K / cw;
+    return gather<kGatherU, 4>(
+        M * K4, [&](int i) { return src + (size_t)(i / K4) * src_stride + 4 * (i % K4); },
+        [&](int i, const float (&v)[4]) {
+          *reinterpret_cast<float4*>(dst + (i / K4) * K + act_pos(4 * (i % K4), cw, nvt)) =
+              make_float4(v[0], v[1], v[2], v[3]);
+        },
+        oi, 9);
   }
 
   // xres[i][m] = x_m[a + i] for the CTA's rows [a, b): the residual input of the op.
-  __device__ bool load_residual(const OpDesc& op, float* xres, int a, int b, int M, int oi) {
-    bool ok = true;
-    for (int t = tid; t < (b - a) * M; t += kConsumerThreads) {
-      const int i = t / M, m = t % M;
-      float v = 0.f;
-      ok &= load_x1(op, m, a + i, v, oi);
-      xres[t] = v;
-    }
-    return ok;
+  __device__ __forceinline__ bool load_residual(const OpDesc& op, float* xres, int a, int b, int M, int oi) {
+    const int n = (b - a) * M;
+    if (op.xsrc == X_F32)
+      return gather<2, 1>(
+          n, [&](int t) { return x_tagged(op, t % M) + a + t / M; },
+          [&](int t, const float (&v)[1]) { xres[t] = v[0]; }, oi, 8);
+    for (int t = tid; t < n; t += kConsumerThreads)
+      xres[t] = __uint_as_float((uint32_t)__ldg(x_bf16(op, t % M) + a + t / M) << 16);
+    return true;
   }
 
   // ---------------------------------------------------------------- routing (MoE layers)
@@ -846,16 +1065,13 @@ struct Consumer {
   // top-k per token (largest first, lower index on ties), softmax over the selected logits,
   // and the union of the window's experts (shared experts first). The producer lanes read it
   // from shared memory once flags[kFlagRoute] names the layer. Uses the start of s.act.
-  __device__ __noinline__ bool ensure_routing(const OpDesc& op, int M, int oi) {
+  __device__ __forceinline__ bool ensure_routing(const OpDesc& op, int M, int oi) {
     if (s.flags[kFlagRoute] == op.layer + 1) return true;
     const int E = p.E, k = p.top_k;
     float* r = s.act;  // [M][E]
-    bool ok = true;
-    for (int i = tid; i < M * E; i += kConsumerThreads) {
-      float v = 0.f;
-      ok &= poll1(p, op.act + i, tag, v, oi, 10);
-      r[i] = v;
-    }
+    if (!wait_counter(op.aux_ctr, p.n_ctas, oi, 10)) return false;
+    const bool ok = gather<4, 1>(
+        M * E, [&](int i) { return op.act + i; }, [&](int i, const float (&v)[1]) { r[i] = v[0]; }, oi, 10);
     if (!consumer_all(ok)) return false;
     RouteBlock* rb = s.route;
     for (int m = 0; m < M; ++m) {
@@ -944,9 +1160,11 @@ struct Consumer {
   // ---------------------------------------------------------------- matrix ops
   // This warp's tiles of a matrix op. Results of a row group land in lane j*MT + m (row j,
   // token m); tokens m >= M (MT = 4 serving a 2- or 3-token window) are computed on zero
-  // activations and dropped.
-  template <int WT, int MT, int NR>
-  __device__ __noinline__ bool gemv_op_t(int oi, const OpDesc& op, int M, float* xres, int a, float* accd) {
+  // activations and dropped. NI > 0 (one token, whole rows): the warp keeps the op's
+  // activations in NI chunks of registers per lane for the whole op; a separate instantiation,
+  // so the shared-memory path's registers never sit next to them.
+  template <int WT, int MT, int NR, int NI>
+  __device__ __forceinline__ bool gemv_op_t(int oi, const OpDesc& op, int M, float* xres, int a, float* accd) {
     GemvIter it;
     const bool routed = op.type == OP_ROUTED_GATEUP || op.type == OP_EXP_DOWN;
     const int n_slots = routed ? s.route->n_slots : 0;
@@ -959,12 +1177,9 @@ struct Consumer {
     Tile t;
     bool ok = true;
     const int i = lane / MT, m = lane % MT;
-    // one token, whole rows, activations that fit: keep them in registers for the whole op
-    constexpr int NI = RegCfg<WT>::NI;
-    const bool regs = MT == 1 && op.type != OP_EXP_DOWN && op.Kc == op.K && op.K <= 32 * NI * WCfg<WT>::CW;
-    ActRegs<WT, (MT == 1 ? NI : 1)> AR;
-    if constexpr (MT == 1)
-      if (regs) act_regs_load(AR, s.act, op.K, 0, op.K, lane);
+    static_assert(NI == 0 || MT == 1, "register activations serve one token");
+    ActRegs<WT, (NI > 0 ? NI : 1)> AR;
+    if constexpr (NI > 0) act_regs_load(AR, s.act, op.K, 0, op.K, lane);
     while (it.next(t)) {
       uint8_t* slot;
       uint32_t eb;
@@ -973,14 +1188,10 @@ struct Consumer {
         break;
       }
       const float* actp = (op.type == OP_EXP_DOWN && op.stage_all) ? s.act + (size_t)t.sl * M * op.K : s.act;
-      if constexpr (MT == 1) {
-        if (regs)
-          warp_gemv_reg<WT, NR, NI>(slot, t.nr, t.kn, AR, A, lane);
-        else
-          warp_gemv<WT, MT, NR>(slot, t.nr, t.kn, t.kc, actp, op.K, M, A, lane);
-      } else {
+      if constexpr (NI > 0)
+        warp_gemv_reg<WT, NR, NI>(slot, t.nr, t.kn, AR, A, lane);
+      else
         warp_gemv<WT, MT, NR>(slot, t.nr, t.kn, t.kc, actp, op.K, M, A, lane);
-      }
       release(eb);
       if (!t.last_k) continue;
       const float v = warp_rowsums<NR, MT>(A, t.nr, lane);
@@ -1038,17 +1249,17 @@ struct Consumer {
   }
 
   // Column split: every warp covers all of the CTA's rows over its own column range, keeps its
-  // activations in registers (one token) and leaves a partial sum per row; the warps' partials
-  // are added in warp order afterwards (csplit_epilogue).
-  template <int WT, int MT, int NR>
-  __device__ __noinline__ bool gemv_csplit_t(int oi, const OpDesc& op, int M, int a, float* parts) {
+  // activations in registers (one token, NI chunks per lane) and leaves a partial sum per row;
+  // the warps' partials are added in warp order afterwards (csplit_epilogue).
+  template <int WT, int MT, int NR, int NI>
+  __device__ __forceinline__ bool gemv_csplit_t(int oi, const OpDesc& op, int M, int a, float* parts) {
     GemvIter it;
     it.init(op, p.n_ctas, blockIdx.x, warp, 0, nullptr, 0);
     Acc<NR, MT> A;
-    constexpr int NI = RegCfg<WT>::NI;
-    ActRegs<WT, (MT == 1 ? NI : 1)> AR;
-    if constexpr (MT == 1)
-      if (it.kw0 < it.kw1) act_regs_load(AR, s.act, op.K, it.kw0, it.kw1 - it.kw0, lane);
+    static_assert(NI == 0 || MT == 1, "register activations serve one token");
+    ActRegs<WT, (NI > 0 ? NI : 1)> AR;
+    if constexpr (NI > 0)
+      act_regs_load(AR, s.act, op.K, it.kw0, max(0, it.kw1 - it.kw0), lane);  // unconditional: no spills
     const int rows = it.bw - it.aw;
     Tile t;
     while (it.next(t)) {
@@ -1056,7 +1267,7 @@ struct Consumer {
       uint32_t eb;
       if (!next_slot(oi, slot, eb)) return false;
       acc_zero(A);
-      if constexpr (MT == 1)
+      if constexpr (NI > 0)
         warp_gemv_reg<WT, NR, NI>(slot, t.nr, t.kn, AR, A, lane);
       else
         warp_gemv<WT, MT, NR>(slot, t.nr, t.kn, t.kc, s.act, op.K, M, A, lane);
@@ -1097,28 +1308,62 @@ struct Consumer {
     }
   }
 
-  // Tile rows per warp-tile template: bf16 2/4/8, FP8 4/8, MXFP4 8 (the host's R fits).
+  // Instantiations: tile rows NR (bf16 2/4/8, FP8 4/8, MXFP4 8; the host's R fits) and, for
+  // one token, the register chunks NI the warp's columns need (0: activations stay in shared
+  // memory). The host only makes column-split ops whose columns fit in registers.
   template <int MT>
   __device__ bool gemv_dispatch(int oi, const OpDesc& op, int M, float* xres, int a, float* accd) {
-    if (op.csplit) {
-      if (op.wtype == W_BF16) return gemv_csplit_t<W_BF16, MT, 8>(oi, op, M, a, accd);
-      return gemv_csplit_t<W_FP8, MT, 8>(oi, op, M, a, accd);
-    }
+    const int kw = op.csplit ? op.Kc : op.K;  // columns one warp multiplies
+    const bool whole = op.csplit || (op.Kc == op.K && op.type != OP_EXP_DOWN);
     if (op.wtype == W_BF16) {
-      if (op.R <= 2) return gemv_op_t<W_BF16, MT, 2>(oi, op, M, xres, a, accd);
-      if (op.R <= 4) return gemv_op_t<W_BF16, MT, 4>(oi, op, M, xres, a, accd);
-      return gemv_op_t<W_BF16, MT, 8>(oi, op, M, xres, a, accd);
+      const int ni = (MT == 1 && whole) ? (kw <= 32 * 4 * 8 ? 4 : (kw <= 32 * 10 * 8 ? 10 : 0)) : 0;
+      if (op.csplit) {
+        if constexpr (MT == 1) {
+          if (ni == 4) return gemv_csplit_entry<W_BF16, 1, 8, 4>(p, oi, op, M, a, accd);
+          return gemv_csplit_entry<W_BF16, 1, 8, 10>(p, oi, op, M, a, accd);
+        } else {
+          return gemv_csplit_entry<W_BF16, MT, 8, 0>(p, oi, op, M, a, accd);
+        }
+      }
+      if constexpr (MT == 1) {
+        if (ni == 4) {
+          if (op.R <= 2) return gemv_tiles_entry<W_BF16, 1, 2, 4>(p, oi, op, M, xres, a, accd);
+          if (op.R <= 4) return gemv_tiles_entry<W_BF16, 1, 4, 4>(p, oi, op, M, xres, a, accd);
+          return gemv_tiles_entry<W_BF16, 1, 8, 4>(p, oi, op, M, xres, a, accd);
+        }
+        if (ni == 10) {
+          if (op.R <= 2) return gemv_tiles_entry<W_BF16, 1, 2, 10>(p, oi, op, M, xres, a, accd);
+          if (op.R <= 4) return gemv_tiles_entry<W_BF16, 1, 4, 10>(p, oi, op, M, xres, a, accd);
+          return gemv_tiles_entry<W_BF16, 1, 8, 10>(p, oi, op, M, xres, a, accd);
+        }
+      }
+      if (op.R <= 2) return gemv_tiles_entry<W_BF16, MT, 2, 0>(p, oi, op, M, xres, a, accd);
+      if (op.R <= 4) return gemv_tiles_entry<W_BF16, MT, 4, 0>(p, oi, op, M, xres, a, accd);
+      return gemv_tiles_entry<W_BF16, MT, 8, 0>(p, oi, op, M, xres, a, accd);
     }
     if (op.wtype == W_FP8) {
-      if (op.R <= 4) return gemv_op_t<W_FP8, MT, 4>(oi, op, M, xres, a, accd);
-      return gemv_op_t<W_FP8, MT, 8>(oi, op, M, xres, a, accd);
+      const bool regs = MT == 1 && whole && kw <= 32 * 5 * 16;
+      if (op.csplit) {
+        if constexpr (MT == 1) return gemv_csplit_entry<W_FP8, 1, 8, 5>(p, oi, op, M, a, accd);
+        else return gemv_csplit_entry<W_FP8, MT, 8, 0>(p, oi, op, M, a, accd);
+      }
+      if constexpr (MT == 1) {
+        if (regs) {
+          if (op.R <= 4) return gemv_tiles_entry<W_FP8, 1, 4, 5>(p, oi, op, M, xres, a, accd);
+          return gemv_tiles_entry<W_FP8, 1, 8, 5>(p, oi, op, M, xres, a, accd);
+        }
+      }
+      if (op.R <= 4) return gemv_tiles_entry<W_FP8, MT, 4, 0>(p, oi, op, M, xres, a, accd);
+      return gemv_tiles_entry<W_FP8, MT, 8, 0>(p, oi, op, M, xres, a, accd);
     }
-    return gemv_op_t<W_MXFP4, MT, 8>(oi, op, M, xres, a, accd);
+    if constexpr (MT == 1)
+      if (whole && kw <= 32 * 3 * 32) return gemv_tiles_entry<W_MXFP4, 1, 8, 3>(p, oi, op, M, xres, a, accd);
+    return gemv_tiles_entry<W_MXFP4, MT, 8, 0>(p, oi, op, M, xres, a, accd);
   }
 
   // Expert down, one slot (its hidden vectors staged in act by the caller).
   template <int MT>
-  __device__ __noinline__ bool gemv_slot(int oi, const OpDesc& op, int sl, int M, int a, float* accd) {
+  __device__ __forceinline__ bool gemv_slot(int oi, const OpDesc& op, int sl, int M, int a, float* accd) {
     int ca, cb, aw, bw;
     cta_rows(op.N, op.unit, p.n_ctas, blockIdx.x, ca, cb);
     warp_rows(ca, cb, op.unit, warp, aw, bw);
@@ -1140,85 +1385,120 @@ struct Consumer {
     return true;
   }
 
-  __device__ bool gemv_op(int oi, const OpDesc& op, int M, const uint2 (&gpre)[kGainPre]) {
-    const int C = p.n_ctas, cta = blockIdx.x;
-    const int cw = chunk_width(op.wtype);
-    int a = 0, b = 0;
-    float* xres = nullptr;
-    float* accd = nullptr;
-    bool ok = true;
-    // prologue: poll the activations every tile multiplies, and the residual rows of this CTA
+  // Rows [a, b) of the CTA, and where its residual rows (xres) and partial sums (accd) sit in
+  // s.act; the same in all three phases of a matrix op.
+  struct GemvGeo {
+    int a, b;
+    float* xres;
+    float* accd;
+  };
+  __device__ __forceinline__ GemvGeo gemv_geo(const OpDesc& op, int M) const {
+    GemvGeo g{0, 0, nullptr, nullptr};
     switch (op.type) {
       case OP_OPROJ:
       case OP_DOWN:
-        cta_rows(op.N, op.unit, C, cta, a, b);
-        ok &= copy_act(s.act, op.act, M, op.K, op.K, cw, oi);
-        xres = s.act + M * op.K;
-        ok &= load_residual(op, xres, a, b, M, oi);
-        if (op.csplit) accd = xres + (b - a) * M;  // per-warp partial sums
+        cta_rows(op.N, op.unit, p.n_ctas, blockIdx.x, g.a, g.b);
+        g.xres = s.act + M * op.K;
+        if (op.csplit) g.accd = g.xres + (g.b - g.a) * M;  // per-warp partial sums
         break;
       case OP_EXP_DOWN: {
-        if (!ensure_routing(op, M, oi)) return false;
-        cta_rows(op.N, op.unit, C, cta, a, b);
-        const int n_slots = s.route->n_slots;
-        const int hfl = op.stage_all ? n_slots * M * op.K : M * op.K;
-        xres = s.act + hfl;
-        accd = xres + (b - a) * M;
-        ok &= load_residual(op, xres, a, b, M, oi);
-        for (int t = tid; t < (b - a) * M; t += kConsumerThreads) accd[t] = 0.f;
-        if (op.stage_all)
-          for (int sl = 0; sl < n_slots; ++sl)
-            ok &= copy_act(s.act + (size_t)sl * M * op.K, op.eh + (size_t)sl * p.Mmax * op.K, M, op.K, op.K, cw, oi);
+        cta_rows(op.N, op.unit, p.n_ctas, blockIdx.x, g.a, g.b);
+        const int hfl = op.stage_all ? s.route->n_slots * M * op.K : M * op.K;
+        g.xres = s.act + hfl;
+        g.accd = g.xres + (g.b - g.a) * M;
         break;
       }
-      case OP_ROUTED_GATEUP:
-        if (!ensure_routing(op, M, oi)) return false;
-        ok &= norm_prologue(op, M, gpre, oi);
+      default:
+        if (op.csplit) {
+          cta_rows(op.N, op.unit, p.n_ctas, blockIdx.x, g.a, g.b);
+          g.accd = s.act + M * op.K;  // per-warp partial sums
+        }
+        break;
+    }
+    return g;
+  }
+
+  // Phase 1 of a matrix op: wait for its input, then poll the activations every tile multiplies
+  // and the residual rows of this CTA into shared memory.
+  __device__ __forceinline__ bool gemv_prologue(int oi, const OpDesc& op, int M) {
+    // the gain is a weight: load it before waiting for the input
+    uint2 gpre[kGainPre];
+    load_gain(op, gpre);
+    if (op.wait_ctr >= 0 && !wait_counter(op.wait_ctr, op.wait_n, oi, 4)) return false;
+    if (tid == 0) TRACE(p, oi, 1, gtimer());
+    if ((op.type == OP_ROUTED_GATEUP || op.type == OP_EXP_DOWN) && !routing_entry(p, oi, M)) return false;
+    const int cw = chunk_width(op.wtype);
+    const GemvGeo g = gemv_geo(op, M);
+    bool ok = true;
+    switch (op.type) {
+      case OP_OPROJ:
+      case OP_DOWN:
+        ok &= copy_act(s.act, op.act, M, op.K, op.K, cw, oi);
+        if (tid == 0) TRACE(p, oi, 8, gtimer());
+        ok &= load_residual(op, g.xres, g.a, g.b, M, oi);
+        break;
+      case OP_EXP_DOWN:
+        ok &= load_residual(op, g.xres, g.a, g.b, M, oi);
+        for (int t = tid; t < (g.b - g.a) * M; t += kConsumerThreads) g.accd[t] = 0.f;
+        if (op.stage_all)
+          for (int sl = 0; sl < s.route->n_slots; ++sl)
+            ok &= copy_act(s.act + (size_t)sl * M * op.K, op.eh + (size_t)sl * p.Mmax * op.K, M, op.K, op.K, cw, oi);
         break;
       default:
         ok &= norm_prologue(op, M, gpre, oi);
-        if (op.csplit) {
-          cta_rows(op.N, op.unit, C, cta, a, b);
-          accd = s.act + M * op.K;  // per-warp partial sums
-        }
         break;
     }
     if (!consumer_all(ok)) return false;
     if (tid == 0) {
-      TRACE(p, oi, 1, gtimer());
       TRACE(p, oi, 2, gtimer());
+      TRACE(p, oi, 9, (uint64_t)s.flags[kFlagLate]);
     }
+    return true;
+  }
+
+  // Phase 2: every warp's tiles (out-of-line tile loops).
+  __device__ __forceinline__ bool gemv_tiles(int oi, const OpDesc& op, int M) {
+    const GemvGeo g = gemv_geo(op, M);
     if (op.type == OP_EXP_DOWN && !op.stage_all) {
       // one slot at a time: stage its hidden vectors, then every warp runs its rows of it
-      const int n_slots = s.route->n_slots;
+      const int n_slots = s.route->n_slots, cw = chunk_width(op.wtype);
       for (int sl = 0; sl < n_slots; ++sl) {
-        ok = copy_act(s.act, op.eh + (size_t)sl * p.Mmax * op.K, M, op.K, op.K, cw, oi);
+        const bool ok = copy_act_entry(p, oi, s.act, op.eh + (size_t)sl * p.Mmax * op.K, M, op.K, op.K, cw);
         if (!consumer_all(ok)) return false;
-        const bool r = M == 1 ? gemv_slot<1>(oi, op, sl, M, a, accd) : gemv_slot<4>(oi, op, sl, M, a, accd);
+        const bool r = M == 1 ? gemv_slot_entry<1>(p, oi, op, sl, M, g.a, g.accd)
+                              : gemv_slot_entry<4>(p, oi, op, sl, M, g.a, g.accd);
         if (!consumer_all(r)) return false;
       }
     } else {
-      const bool r = M == 1 ? gemv_dispatch<1>(oi, op, M, xres, a, accd) : gemv_dispatch<4>(oi, op, M, xres, a, accd);
+      const bool r = M == 1 ? gemv_dispatch<1>(oi, op, M, g.xres, g.a, g.accd)
+                            : gemv_dispatch<4>(oi, op, M, g.xres, g.a, g.accd);
       if (!consumer_all(r)) return false;
     }
     if (tid == 0) TRACE(p, oi, 3, gtimer());
-    if (op.csplit) csplit_epilogue(op, M, a, b, xres, accd);
+    return true;
+  }
+
+  // Phase 3: outputs that need every warp's results (column-split sums, expert-down residual
+  // stores, the LM head's argmax) and the router's routing.
+  __device__ __forceinline__ bool gemv_epilogue(int oi, const OpDesc& op, int M) {
+    const GemvGeo g = gemv_geo(op, M);
+    if (op.csplit) csplit_epilogue(op, M, g.a, g.b, g.xres, g.accd);
     if (op.type == OP_EXP_DOWN) {
-      for (int t = tid; t < (b - a) * M; t += kConsumerThreads) {
+      for (int t = tid; t < (g.b - g.a) * M; t += kConsumerThreads) {
         const int i = t / M, m = t % M;
-        st_tagged(op.x_out + (size_t)m * p.H + a + i, xres[t] + accd[t], tag);
+        st_tagged(op.x_out + (size_t)m * p.H + g.a + i, g.xres[t] + g.accd[t], tag);
       }
     }
     if (op.type == OP_ROUTER) {
-      consumer_sync();  // s.act is reused for the logits
-      return ensure_routing(op, M, oi);
+      arrive(op.ctr);  // before the routing, which waits for every CTA's logits
+      return routing_entry(p, oi, M);
     }
     if (op.type == OP_LMHEAD) lmhead_finish(op, M);
     return true;
   }
 
   // Per-warp bests -> per-CTA partial -> the last CTA reduces all partials (lowest index on ties).
-  __device__ __noinline__ void lmhead_finish(const OpDesc& op, int M) {
+  __device__ __forceinline__ void lmhead_finish(const OpDesc& op, int M) {
     consumer_sync();
     const int MT = M == 1 ? 1 : 4;  // lane l of a warp tracked token l % MT
     if (tid < M) {
@@ -1255,7 +1535,9 @@ struct Consumer {
 
   // ---------------------------------------------------------------- attention op
   template <int G_>
-  __device__ __noinline__ bool attn_op(int oi, const OpDesc& op, int pos, int M) {
+  __device__ __forceinline__ bool attn_op(int oi, const OpDesc& op, int pos, int M) {
+    if (op.wait_ctr >= 0 && !wait_counter(op.wait_ctr, op.wait_n, oi, 4)) return false;
+    if (tid == 0) TRACE(p, oi, 1, gtimer());
     const int P = s.slot_bytes / 512;
     const int G = G_, MG = M * G, ns = p.ns_max;
     const AttnScratch a = attn_scratch(p, s, M, P);
@@ -1268,38 +1550,48 @@ struct Consumer {
     const uint64_t* qkv = op.act;
     const size_t sstride = (size_t)p.Mmax * G * kPart;  // words per split partial
     uint64_t* lpart = p.part + (size_t)op.layer * p.n_kv * ns * sstride;
+    const int GR = (G + 2) * 32;  // float4 groups of one token's q, k, v rows of the kv group
     for (; it.j < it.nsplit; it.next_split()) {
       int head, sidx, p0, p1;
       split_range(it.S, ns, it.j, head, sidx, p0, p1);
-      // CTA prologue: rotated, scaled queries of the group; this call's own keys/values
-      bool ok = true;
+      const int nb = max(p0, pos), nn = max(0, p1 - nb);  // this call's own rows in the split
+      // CTA prologue: poll the group's q (and, for the split holding this call's rows, k and v)
+      // in one batch; rotate and scale the queries; round, keep and append the own rows
+      const int per_m = nn > 0 ? GR : G * 32;
+      bool ok = gather<4, 4>(
+          M * per_m,
+          [&](int i) {
+            const int m = i / per_m, r = i - m * per_m;
+            const uint64_t* row = qkv + (size_t)m * p.qkv_rows;
+            if (r < G * 32) return row + head * G * 128 + 4 * r;
+            if (r < (G + 1) * 32) return row + (p.n_q + head) * 128 + 4 * (r - G * 32);
+            return row + (p.n_q + p.n_kv + head) * 128 + 4 * (r - (G + 1) * 32);
+          },
+          [&](int i, const float (&v)[4]) {
+            const int m = i / per_m, r = i - m * per_m;
+            *reinterpret_cast<float4*>(a.raw + (m * GR + r) * 4) = make_float4(v[0], v[1], v[2], v[3]);
+          },
+          oi, 11);
+      if (!consumer_all(ok)) return false;
       for (int idx = tid; idx < MG * 64; idx += kConsumerThreads) {
         const int mh = idx >> 6, i = idx & 63;
-        const int m = mh / G, h = head * G + mh % G;
-        const uint64_t* qr = qkv + (size_t)m * p.qkv_rows + h * 128;
-        float x1 = 0.f, x2 = 0.f;
-        ok &= poll1(p, qr + i, tag, x1, oi, 11);
-        ok &= poll1(p, qr + i + 64, tag, x2, oi, 11);
+        const int m = mh / G;
+        const float* qr = a.raw + m * GR * 4 + (mh % G) * 128;
+        const float x1 = qr[i], x2 = qr[i + 64];
         const float2 cs = s.rope[m * 64 + i];
         a.q[mh * 128 + i] = (x1 * cs.x - x2 * cs.y) * qscale;
         a.q[mh * 128 + i + 64] = (x1 * cs.y + x2 * cs.x) * qscale;
       }
-      const int nb = max(p0, pos), nn = max(0, p1 - nb);
       for (int idx = tid; idx < nn * 64; idx += kConsumerThreads) {
         const int r = idx >> 6, i = idx & 63;
         const int m = nb - pos + r;
-        const uint64_t* kr = qkv + (size_t)m * p.qkv_rows + (p.n_q + head) * 128;
-        const uint64_t* vr = qkv + (size_t)m * p.qkv_rows + (p.n_q + p.n_kv + head) * 128;
-        float k1 = 0.f, k2 = 0.f, v1 = 0.f, v2 = 0.f;
-        ok &= poll1(p, kr + i, tag, k1, oi, 12);
-        ok &= poll1(p, kr + i + 64, tag, k2, oi, 12);
-        ok &= poll1(p, vr + i, tag, v1, oi, 12);
-        ok &= poll1(p, vr + i + 64, tag, v2, oi, 12);
+        const float* kr = a.raw + m * GR * 4 + G * 128;
+        const float* vr = kr + 128;
         const float2 cs = s.rope[m * 64 + i];
-        const uint16_t b1 = __bfloat16_as_ushort(__float2bfloat16_rn(k1 * cs.x - k2 * cs.y));
-        const uint16_t b2 = __bfloat16_as_ushort(__float2bfloat16_rn(k1 * cs.y + k2 * cs.x));
-        const uint16_t c1 = __bfloat16_as_ushort(__float2bfloat16_rn(v1));
-        const uint16_t c2 = __bfloat16_as_ushort(__float2bfloat16_rn(v2));
+        const uint16_t b1 = __bfloat16_as_ushort(__float2bfloat16_rn(kr[i] * cs.x - kr[i + 64] * cs.y));
+        const uint16_t b2 = __bfloat16_as_ushort(__float2bfloat16_rn(kr[i] * cs.y + kr[i + 64] * cs.x));
+        const uint16_t c1 = __bfloat16_as_ushort(__float2bfloat16_rn(vr[i]));
+        const uint16_t c2 = __bfloat16_as_ushort(__float2bfloat16_rn(vr[i + 64]));
         a.kvn[r * 128 + i] = b1;
         a.kvn[r * 128 + i + 64] = b2;
         a.kvn[(nn + r) * 128 + i] = c1;
@@ -1310,9 +1602,8 @@ struct Consumer {
         op.vc[off + i] = c1;
         op.vc[off + i + 64] = c2;
       }
-      if (!consumer_all(ok)) return false;
+      consumer_sync();
       if (tid == 0 && it.j == (int)blockIdx.x) {
-        TRACE(p, oi, 1, gtimer());
         TRACE(p, oi, 2, gtimer());
       }
       // per warp: token m_tok's G heads over this warp's share of the cached rows
@@ -1359,27 +1650,33 @@ struct Consumer {
       }
       if (!consumer_all(ok)) return false;
       if (tid == 0) TRACE(p, oi, 3, gtimer());
+      // the split's partial, every word tagged (the two pad words too: the merge polls the
+      // (max, sum) pair as one 4-word item)
       uint64_t* part = lpart + (size_t)(head * ns + sidx) * sstride;
       for (int idx = tid; idx < MG * kPart; idx += kConsumerThreads) {
         const int mh = idx / kPart, e = idx % kPart;
-        if (e == 2 || e == 3) continue;
         const int m = mh / G, h = mh % G;
-        float mx = -INFINITY;
-        for (int w = m; w < kConsumerWarps; w += M) mx = fmaxf(mx, a.mg[(w * G + h) * kPart]);
-        float l = 0.f, o = 0.f;
-        for (int w = m; w < kConsumerWarps; w += M) {
-          const float mw = a.mg[(w * G + h) * kPart];
-          const float f = mw == -INFINITY ? 0.f : exp2f(mw - mx);
-          l += f * a.mg[(w * G + h) * kPart + 1];
-          if (e >= 4) o += f * a.mg[(w * G + h) * kPart + e];
+        float val = 0.f;
+        if (e != 2 && e != 3) {
+          float mx = -INFINITY;
+          for (int w = m; w < kConsumerWarps; w += M) mx = fmaxf(mx, a.mg[(w * G + h) * kPart]);
+          float l = 0.f, o = 0.f;
+          for (int w = m; w < kConsumerWarps; w += M) {
+            const float mw = a.mg[(w * G + h) * kPart];
+            const float f = mw == -INFINITY ? 0.f : exp2f(mw - mx);
+            l += f * a.mg[(w * G + h) * kPart + 1];
+            if (e >= 4) o += f * a.mg[(w * G + h) * kPart + e];
+          }
+          val = e == 0 ? mx : (e == 1 ? l : o);
         }
-        st_tagged(part + mh * kPart + e, e == 0 ? mx : (e == 1 ? l : o), tag);
+        st_tagged(part + mh * kPart + e, val, tag);
       }
-      consumer_sync();
+      arrive(op.aux_ctr + head);
     }
     // Phase 2: the splits of a kv head merge its outputs together, each split a 1/ns slice
-    // (log-sum-exp in base 2), polling the head's tagged partials. Every split of this CTA was
-    // published above before any of these polls, so no CTA waits on one that waits on it.
+    // (log-sum-exp in base 2). One batch polls every split's (max, sum) of the slice's rows and
+    // its share of the outputs. Every split of this CTA was published above before these polls,
+    // so no CTA waits on one that waits on it.
     AttnIter it2;
     it2.init(p, blockIdx.x, warp, pos, M, P);
     for (; it2.j < it2.nsplit; it2.next_split()) {
@@ -1390,59 +1687,74 @@ struct Consumer {
       const int o0 = (int)((long long)total * sidx / ns), o1 = (int)((long long)total * (sidx + 1) / ns);
       if (o0 >= o1) continue;
       const int mhA = o0 >> 5, mhB = (o1 - 1) >> 5;
-      bool ok = true;
-      // weights of every split for the (m, h) rows of this slice (sums parked in mg)
-      for (int mh = mhA + warp; mh <= mhB; mh += kConsumerWarps) {
-        float* cw = a.cw + (mh - mhA) * ns;
-        float* lw = a.mg + (mh - mhA) * ns;
+      const int nrow = mhB - mhA + 1, nout = o1 - o0, per = nrow + nout;
+      float4* outs = reinterpret_cast<float4*>(a.sc);  // [ns][nout]
+      if (tid == 0) TRACE(p, oi, 10, gtimer());
+      if (!wait_counter(op.aux_ctr + head, ns, oi, 13)) return false;
+      if (tid == 0) TRACE(p, oi, 11, gtimer());
+      bool ok = gather<4, 4>(
+          ns * per,
+          [&](int i) {
+            const int q2 = i / per, k = i - q2 * per;
+            const uint64_t* sp = hp + q2 * sstride;
+            if (k < nrow) return sp + (mhA + k) * kPart;
+            const int oo = o0 + k - nrow;
+            return sp + (oo >> 5) * kPart + 4 + 4 * (oo & 31);
+          },
+          [&](int i, const float (&v)[4]) {
+            const int q2 = i / per, k = i - q2 * per;
+            if (k < nrow)
+              a.ml[q2 * nrow + k] = make_float2(v[0], v[1]);
+            else
+              outs[q2 * nout + k - nrow] = make_float4(v[0], v[1], v[2], v[3]);
+          },
+          oi, 13);
+      if (!consumer_all(ok)) return false;
+      // weights of every split for each row of the slice (one warp per row)
+      for (int r = warp; r < nrow; r += kConsumerWarps) {
+        float* cw = a.cw + r * ns;
         float mx = -INFINITY;
-        for (int q2 = lane; q2 < ns; q2 += 32) {
-          float mq = 0.f, lq = 0.f;
-          ok &= poll1(p, hp + q2 * sstride + mh * kPart, tag, mq, oi, 13);
-          ok &= poll1(p, hp + q2 * sstride + mh * kPart + 1, tag, lq, oi, 13);
-          cw[q2] = mq;
-          lw[q2] = lq;
-          mx = fmaxf(mx, mq);
-        }
+        for (int q2 = lane; q2 < ns; q2 += 32) mx = fmaxf(mx, a.ml[q2 * nrow + r].x);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         float l = 0.f;
         for (int q2 = lane; q2 < ns; q2 += 32) {
-          const float mq = cw[q2];
-          const float w = mq == -INFINITY ? 0.f : exp2f(mq - mx);
+          const float2 ml = a.ml[q2 * nrow + r];
+          const float w = ml.x == -INFINITY ? 0.f : exp2f(ml.x - mx);
           cw[q2] = w;
-          l += w * lw[q2];
+          l += w * ml.y;
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
         const float inv = 1.0f / l;
         for (int q2 = lane; q2 < ns; q2 += 32) cw[q2] *= inv;
       }
-      if (!consumer_all(ok)) return false;
-      // one (output, split) product per thread, then a fixed-order sum over the splits
-      float4* prod = reinterpret_cast<float4*>(a.sc);
-      const int n = (o1 - o0) * ns;
-      for (int t = tid; t < n; t += kConsumerThreads) {
-        const int oo = o0 + t / ns, q2 = t % ns;
-        const int mh = oo >> 5, d4 = oo & 31;
-        const float w = a.cw[(mh - mhA) * ns + q2];
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        ok &= poll4(p, hp + q2 * sstride + mh * kPart + 4 + 4 * d4, tag, v, oi, 14);
-        prod[t] = make_float4(w * v.x, w * v.y, w * v.z, w * v.w);
-      }
-      if (!consumer_all(ok)) return false;
-      for (int t = tid; t < o1 - o0; t += kConsumerThreads) {
+      consumer_sync();
+      // each output vector: a warp sums the splits' weighted slices (lanes over splits, then a
+      // fixed butterfly)
+      for (int k = warp; k < nout; k += kConsumerWarps) {
+        const int oo = o0 + k, mh = oo >> 5, d4 = oo & 31;
+        const float* cw = a.cw + (mh - mhA) * ns;
         float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int q2 = 0; q2 < ns; ++q2) {
-          const float4 v = prod[t * ns + q2];
-          o.x += v.x;
-          o.y += v.y;
-          o.z += v.z;
-          o.w += v.w;
+        for (int q2 = lane; q2 < ns; q2 += 32) {
+          const float w = cw[q2];
+          const float4 v = outs[q2 * nout + k];
+          o.x = fmaf(w, v.x, o.x);
+          o.y = fmaf(w, v.y, o.y);
+          o.z = fmaf(w, v.z, o.z);
+          o.w = fmaf(w, v.w, o.w);
         }
-        const int oo = o0 + t, mh = oo >> 5, d4 = oo & 31;
-        const int m = mh / G, h = head * G + mh % G;
-        st_tagged4(op.out + (size_t)m * p.n_q * 128 + h * 128 + d4 * 4, o, tag);
+#pragma unroll
+        for (int sh = 16; sh > 0; sh >>= 1) {
+          o.x += __shfl_xor_sync(0xffffffffu, o.x, sh);
+          o.y += __shfl_xor_sync(0xffffffffu, o.y, sh);
+          o.z += __shfl_xor_sync(0xffffffffu, o.z, sh);
+          o.w += __shfl_xor_sync(0xffffffffu, o.w, sh);
+        }
+        if (lane == 0) {
+          const int m = mh / G, h = head * G + mh % G;
+          st_tagged4(op.out + (size_t)m * p.n_q * 128 + h * 128 + d4 * 4, o, tag);
+        }
       }
       consumer_sync();
     }
@@ -1450,32 +1762,32 @@ struct Consumer {
   }
 
   // ---------------------------------------------------------------- main loop
-  __device__ bool run(int pos, int M) {
+  __device__ __forceinline__ bool run(int pos, int M) {
     for (int oi = p.op_begin; oi < p.op_end; ++oi) {
       {
         const int* src = reinterpret_cast<const int*>(p.ops + oi);
         int* dst = reinterpret_cast<int*>(s.op);
         for (int i = tid; i < (int)(sizeof(OpDesc) / 4); i += kConsumerThreads) dst[i] = __ldg(src + i);
+        if (tid == 0) s.flags[kFlagLate] = 0;
       }
       consumer_sync();
       const OpDesc& op = *s.op;
       if (tid == 0) TRACE(p, oi, 0, gtimer());
-      uint2 gpre[kGainPre];
-      load_gain(op, gpre);
       bool ok;
       if (op.type == OP_ATTN) {
         switch (p.G) {
-          case 1: ok = attn_op<1>(oi, op, pos, M); break;
-          case 2: ok = attn_op<2>(oi, op, pos, M); break;
-          case 4: ok = attn_op<4>(oi, op, pos, M); break;
-          case 5: ok = attn_op<5>(oi, op, pos, M); break;
-          default: ok = attn_op<8>(oi, op, pos, M); break;
+          case 1: ok = attn_entry<1>(p, oi, pos, M); break;
+          case 2: ok = attn_entry<2>(p, oi, pos, M); break;
+          case 4: ok = attn_entry<4>(p, oi, pos, M); break;
+          case 5: ok = attn_entry<5>(p, oi, pos, M); break;
+          default: ok = attn_entry<8>(p, oi, pos, M); break;
         }
       } else {
-        ok = gemv_op(oi, op, M, gpre);
+        ok = gemv_prologue_entry(p, oi, M) && gemv_tiles_dispatch_entry(p, oi, M) && gemv_epilogue_entry(p, oi, M);
       }
       if (!ok) return false;
-      consumer_sync();
+      if (op.type != OP_ROUTER) arrive(op.ctr);  // the router arrives before computing the routing
+      else consumer_sync();
       if (tid == 0) TRACE(p, oi, 4, gtimer());
     }
     if (p.op_end == p.n_ops) {
@@ -1497,28 +1809,89 @@ struct Consumer {
   }
 };
 
+// ------------------------------------------------------------------ out-of-line entries
+// Each op runs in a function of its own, and each tile loop in one more: every one rebuilds its
+// Consumer in registers, so the register allocation of a hot loop is its own.
+template <int WT, int MT, int NR, int NI>
+__device__ __noinline__ bool gemv_tiles_entry(const KParams& p, int oi, const OpDesc& op, int M, float* xres, int a,
+                                              float* accd) {
+  Consumer c(p);
+  const bool ok = c.gemv_op_t<WT, MT, NR, NI>(oi, op, M, xres, a, accd);
+  c.save_tiles();
+  return ok;
+}
+
+template <int WT, int MT, int NR, int NI>
+__device__ __noinline__ bool gemv_csplit_entry(const KParams& p, int oi, const OpDesc& op, int M, int a, float* parts) {
+  Consumer c(p);
+  const bool ok = c.gemv_csplit_t<WT, MT, NR, NI>(oi, op, M, a, parts);
+  c.save_tiles();
+  return ok;
+}
+
+template <int MT>
+__device__ __noinline__ bool gemv_slot_entry(const KParams& p, int oi, const OpDesc& op, int sl, int M, int a,
+                                             float* accd) {
+  Consumer c(p);
+  const bool ok = c.gemv_slot<MT>(oi, op, sl, M, a, accd);
+  c.save_tiles();
+  return ok;
+}
+
+__device__ __noinline__ bool gemv_prologue_entry(const KParams& p, int oi, int M) {
+  Consumer c(p);
+  return c.gemv_prologue(oi, *c.s.op, M);
+}
+
+__device__ __noinline__ bool gemv_tiles_dispatch_entry(const KParams& p, int oi, int M) {
+  Consumer c(p);
+  return c.gemv_tiles(oi, *c.s.op, M);
+}
+
+__device__ __noinline__ bool gemv_epilogue_entry(const KParams& p, int oi, int M) {
+  Consumer c(p);
+  return c.gemv_epilogue(oi, *c.s.op, M);
+}
+
+__device__ __noinline__ bool routing_entry(const KParams& p, int oi, int M) {
+  Consumer c(p);
+  return c.ensure_routing(*c.s.op, M, oi);
+}
+
+__device__ __noinline__ bool copy_act_entry(const KParams& p, int oi, float* dst, const uint64_t* src, int M, int K,
+                                            int src_stride, int cw) {
+  Consumer c(p);
+  return c.copy_act(dst, src, M, K, src_stride, cw, oi);
+}
+
+template <int G_>
+__device__ __noinline__ bool attn_entry(const KParams& p, int oi, int pos, int M) {
+  Consumer c(p);
+  const bool ok = c.attn_op<G_>(oi, *c.s.op, pos, M);
+  c.save_tiles();
+  return ok;
+}
+
 // ------------------------------------------------------------------ kernel
-__global__ void __launch_bounds__(kThreads, 1) dec_megakernel(const KParams p) {
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
+__global__ void __launch_bounds__(kThreads, 1) dec_megakernel(const __grid_constant__ KParams p) {
   Smem s = carve(smem_raw, p);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  __shared__ StepState st;
   if (tid == 0) {
     const uint32_t* src = reinterpret_cast<const uint32_t*>(p.state);
-    uint32_t* dst = reinterpret_cast<uint32_t*>(&st);
+    uint32_t* dst = reinterpret_cast<uint32_t*>(&g_st);
     for (int i = 0; i < (int)(sizeof(StepState) / 4); ++i) dst[i] = __ldcg(src + i);
     for (int i = 0; i < kConsumerWarps * kStages; ++i) {
       mbar_init(smem_addr(&s.full[i]), 1);
       mbar_init(smem_addr(&s.empty[i]), 1);
     }
+    for (int w = 0; w < kConsumerWarps; ++w) s.ntiles[w] = 0;
     s.flags[kFlagRoute] = -1;
     mbar_init_fence();
   }
   __syncthreads();
-  const uint32_t epoch = st.epoch;
-  const int pos = st.pos, M = st.m;
+  const int pos = g_st.pos, M = g_st.m;
   if (warp == kConsumerWarps) {
-    Producer pr{p, s, pos, M};
+    Producer pr{p, s, pos, M, l2_policy_evict_first()};
     pr.run(lane);
     return;
   }
@@ -1531,7 +1904,7 @@ __global__ void __launch_bounds__(kThreads, 1) dec_megakernel(const KParams p) {
     s.rope[t] = make_float2((float)cs, (float)sn);
   }
   consumer_sync();
-  Consumer c{p, s, epoch, epoch + 1u, st, tid, warp, lane, 0u};
+  Consumer c(p);
   c.run(pos, M);
 }
 

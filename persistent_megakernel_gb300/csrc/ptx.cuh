@@ -64,6 +64,22 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 
+// The same copy with an L2 cache policy (createpolicy): weights and KV history stream through
+// L2 once per step, so they are marked evict-first and leave the step's activations resident.
+__device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                              uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
 __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
@@ -84,6 +100,11 @@ __device__ __forceinline__ void red_release(uint32_t* p, uint32_t v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// Arrival with no ordering: the data it announces carries its own tags.
+__device__ __forceinline__ void red_relaxed(uint32_t* p, uint32_t v) {
+  asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t* p, uint32_t v) {
   uint32_t old;
   asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
@@ -96,17 +117,19 @@ __device__ __forceinline__ uint64_t gtimer() {
   return t;
 }
 
-// Barrier of the consumer threads only (the producer warp never joins).
+// Barrier of the consumer threads only (the producer warp never joins). Not .aligned: a
+// thread may arrive from a slow path its warp-mates skipped (a late word, a counter wait), and
+// an aligned barrier reached by a diverged warp is undefined.
 __device__ __forceinline__ void consumer_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
+  asm volatile("barrier.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
 }
 
 // Barrier of the consumers that also ANDs a predicate over them: every thread gets the same
-// verdict, so no consumer can leave a loop that the others stay in.
+// verdict, so no consumer can leave a loop that the others stay in. Not .aligned (see above).
 __device__ __forceinline__ bool consumer_all(bool ok) {
   uint32_t r;
   asm volatile(
-      "{ .reg .pred p, q; setp.ne.u32 p, %1, 0; bar.red.and.pred q, 1, %2, p; selp.u32 %0, 1, 0, q; }"
+      "{ .reg .pred p, q; setp.ne.u32 p, %1, 0; barrier.red.and.pred q, 1, %2, p; selp.u32 %0, 1, 0, q; }"
       : "=r"(r)
       : "r"((uint32_t)ok), "n"(kConsumerThreads)
       : "memory");
@@ -133,13 +156,24 @@ __device__ __forceinline__ void st_tagged4(uint64_t* p, float4 v, uint32_t tag) 
                : "memory");
 }
 
+#ifndef DEC_TAGGED_LD_CG
+#define DEC_TAGGED_LD_CG 1
+#endif
+#if DEC_TAGGED_LD_CG
+// Tagged words are read with plain L2 loads (cache-global, L1 bypassed): unlike strong loads they
+// pipeline, and an aligned 8-byte word is read whole, so its tag vouches for its value. volatile
+// keeps a re-poll from being folded into the first read.
+#define DEC_LD_TAGGED "ld.global.cg"
+#else
+#define DEC_LD_TAGGED "ld.relaxed.gpu.global"
+#endif
 __device__ __forceinline__ void ld_tagged2(const uint64_t* p, uint64_t& a, uint64_t& b) {
-  asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+  asm volatile(DEC_LD_TAGGED ".v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
 }
 
 __device__ __forceinline__ uint64_t ld_tagged(const uint64_t* p) {
   uint64_t a;
-  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(a) : "l"(p) : "memory");
+  asm volatile(DEC_LD_TAGGED ".b64 %0, [%1];" : "=l"(a) : "l"(p) : "memory");
   return a;
 }
 
@@ -148,34 +182,29 @@ __device__ __forceinline__ float value_of(uint64_t w) { return __uint_as_float((
 
 // Two fp32 fused multiply-adds in one instruction: (a.x*b.x + c.x, a.y*b.y + c.y), each rounded
 // as fmaf would.
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-  uint64_t d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;"
-      : "=l"(d)
-      : "l"(*reinterpret_cast<uint64_t*>(&a)), "l"(*reinterpret_cast<uint64_t*>(&b)),
-        "l"(*reinterpret_cast<uint64_t*>(&c)));
-  return *reinterpret_cast<float2*>(&d);
-}
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 // Two e4m3fn codes (low byte = first element) -> two floats; exact (e4m3 is a subset of f16).
 __device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two_bytes) {
-  uint32_t h;
-  asm("{ .reg .b16 t; cvt.u16.u32 t, %1; cvt.rn.f16x2.e4m3x2 %0, t; }" : "=r"(h) : "r"(two_bytes));
-  __half2 hh = *reinterpret_cast<__half2*>(&h);
-  return __half22float2(hh);
+  float2 r;
+  asm("{ .reg .b16 t, lo, hi; .reg .b32 h; cvt.u16.u32 t, %2; cvt.rn.f16x2.e4m3x2 h, t; mov.b32 {lo, hi}, h;"
+      " cvt.f32.f16 %0, lo; cvt.f32.f16 %1, hi; }"
+      : "=f"(r.x), "=f"(r.y)
+      : "r"(two_bytes));
+  return r;
 }
 
 // Two e2m1 codes in one byte (low nibble = first element) -> two floats; exact.
 __device__ __forceinline__ float2 e2m1x2_to_float2(uint32_t byte) {
-  uint32_t h;
-  asm("{ .reg .b8 t; .reg .b16 s; cvt.u16.u32 s, %1; cvt.u8.u16 t, s; cvt.rn.f16x2.e2m1x2 %0, t; }"
-      : "=r"(h)
+  float2 r;
+  asm("{ .reg .b8 t; .reg .b16 s, lo, hi; .reg .b32 h; cvt.u16.u32 s, %2; cvt.u8.u16 t, s;"
+      " cvt.rn.f16x2.e2m1x2 h, t; mov.b32 {lo, hi}, h; cvt.f32.f16 %0, lo; cvt.f32.f16 %1, hi; }"
+      : "=f"(r.x), "=f"(r.y)
       : "r"(byte));
-  __half2 hh = *reinterpret_cast<__half2*>(&h);
-  return __half22float2(hh);
+  return r;
 }
 
 // E8M0 scale code -> 2^(e-127) as float (e = 0 gives the subnormal 2^-127).

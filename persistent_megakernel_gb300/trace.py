@@ -22,7 +22,9 @@ import numpy as np
 
 OP_NAMES = ["qkv", "attn", "oproj", "gateup", "down", "router", "shared_gateup", "routed_gateup", "exp_down",
             "lm_head"]
-FIELDS = ["start", "ready", "prologue", "tiles", "end", "p_first", "p_last", "p_count"]
+FIELDS = ["start", "ready", "prologue", "tiles", "end", "p_first", "p_last", "p_count", "loaded", "late",
+          "merge", "merge_ready"]
+NF = len(FIELDS)
 
 
 def op_types(shape) -> list[str]:
@@ -52,7 +54,7 @@ def region(dec, with_tiles=False):
     if not ptr:
         return None, n_ctas, n_ops
     off = ptr - dec.ws.data_ptr()
-    n = n_ctas * n_ops * 8 * 8 + (CONSUMER_WARPS * TILE_LOG * TILE_STAMPS * 8 if with_tiles else 0)
+    n = n_ctas * n_ops * NF * 8 + (CONSUMER_WARPS * TILE_LOG * TILE_STAMPS * 8 if with_tiles else 0)
     return dec.ws[off:off + n], n_ctas, n_ops
 
 
@@ -68,7 +70,7 @@ def read(dec) -> np.ndarray:
     if r is None:
         raise RuntimeError("the loaded library was built without DEC_TRACE")
     torch.cuda.synchronize()
-    return r.cpu().numpy().view(np.uint64).reshape(n_ctas, n_ops, 8).astype(np.int64)
+    return r.cpu().numpy().view(np.uint64).reshape(n_ctas, n_ops, NF).astype(np.int64)
 
 
 def read_tiles(dec) -> np.ndarray:
@@ -78,7 +80,7 @@ def read_tiles(dec) -> np.ndarray:
     r, n_ctas, n_ops = region(dec, with_tiles=True)
     torch.cuda.synchronize()
     a = r.cpu().numpy().view(np.uint64).astype(np.int64)
-    return a[n_ctas * n_ops * 8:].reshape(CONSUMER_WARPS, TILE_LOG, TILE_STAMPS)
+    return a[n_ctas * n_ops * NF:].reshape(CONSUMER_WARPS, TILE_LOG, TILE_STAMPS)
 
 
 def tile_summary(t: np.ndarray, ghz: float = 2.07) -> dict:
@@ -107,8 +109,13 @@ def summarize(rec: np.ndarray, names: list[str]) -> dict:
         lead = float(np.mean((r[:, :, 0] - r[:, :, 5])[live & has_p]) / 1e3) if np.any(live & has_p) else 0.0
         # latest completion across CTAs of each op instance, relative to the earliest start
         span = [float((r[:, k, 4].max() - r[:, k, 0][r[:, k, 0] > 0].min()) / 1e3) for k in range(len(idx))]
+        has_l = r[:, :, 8] > 0
+        load = float(np.mean((r[:, :, 8] - r[:, :, 1])[live & has_l]) / 1e3) if np.any(live & has_l) else 0.0
+        has_m = r[:, :, 11] > 0
+        merge = float(np.mean((r[:, :, 11] - r[:, :, 10])[live & has_m]) / 1e3) if np.any(live & has_m) else 0.0
         res["ops"][kind] = {
             "count": len(idx), "wait": d(0, 1), "prologue": d(1, 2), "tiles": d(2, 3), "end": d(3, 4),
+            "load": load, "late_words": float(np.mean(r[:, :, 9])), "merge_wait": merge,
             "producer_lead": lead, "tiles_issued": float(np.mean(r[:, :, 7])), "span_all_ctas": float(np.mean(span))}
     return res
 
@@ -138,8 +145,9 @@ def main(argv=None):
     ap.add_argument("--chrome", default="")
     ap.add_argument("--dump", default="", help="save the raw records (.npz)")
     args = ap.parse_args(argv)
-    if os.environ.get("DEC_LIB_VARIANT") != "trace":
-        sys.exit("set DEC_LIB_VARIANT=trace")
+    variant = os.environ.get("DEC_LIB_VARIANT", "")
+    if "trace" not in variant:
+        sys.exit("set DEC_LIB_VARIANT to a build with DEC_TRACE (trace)")
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
     sys.path.insert(0, root)
     import torch
@@ -147,7 +155,8 @@ def main(argv=None):
     from synth import model as sm
     from . import build
     from .model import Decoder
-    build.build(variant="trace")
+    if variant == "trace":
+        build.build(variant="trace")
     s = synth.dense_2b_shape().with_(n_layers=args.layers)
     layers = [sm.layer_weights(s, args.seed, l) for l in range(s.n_layers)]
     head = sm.head_weights(s, args.seed)
