@@ -162,9 +162,11 @@ dec_status dec_debug_buffers(dec_ctx* ctx, const uint64_t** hidden, const uint64
                              const int32_t** routing);
 
 /* Self-timing records of the last call (builds compiled with DEC_TRACE; *records is NULL
-   otherwise): uint64 [n_ctas][n_ops][8] %globaltimer nanoseconds per (CTA, op): consumer op
-   start, input ready, prologue done, all warps' tiles done, op end; producer first issue, last
-   issue, and the count of tiles issued. Zero the region between calls to read one call. */
+   otherwise): uint64 [n_ctas][n_ops][12] per (CTA, op): %globaltimer nanoseconds of consumer
+   op start, input ready, prologue done, all warps' tiles done, op end; producer first issue,
+   last issue, the count of tiles issued; first thread's input loads done, the count of input
+   words re-read because their tag was not current yet, attention merge start, attention merge
+   inputs ready. Zero the region between calls to read one call. */
 dec_status dec_trace_buffer(dec_ctx* ctx, const uint64_t** records, int* n_ctas, int* n_ops);
 
 /* Clear a sticky device error: zeroes the whole workspace (step counters, status word and
