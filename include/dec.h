@@ -179,6 +179,28 @@ dec_status dec_sync(dec_ctx* ctx);
 /* Number of kernel launches the last dec_step / dec_verify issued (1 in persistent mode). */
 int dec_last_launch_count(dec_ctx* ctx);
 
+/* LM head without any allocation, for callers that cannot allocate device memory: code that
+   runs inside a memory pool or arena it does not own, or under an allocator it may not call
+   (cudaMalloc / cudaFree can synchronise the device and fail inside some capture or
+   callback contexts). The paper has no counterpart; it is this library's own addition.
+   logits_dev[m][vocab] (fp32) = W_lm RMSNorm(hidden_dev[i]) (RMSNorm with final_norm_dev when
+   it is non-NULL, eps rms_eps; plain hidden otherwise) and argmax_dev[m] (int32, lowest index
+   among equal maxima), computed by the same kernel a context runs for its LM head.
+   hidden_dev bf16 [m][hidden]; w_values_dev / w_scales_dev the dec_pack layout of dtype
+   (DEC_BF16: scales unused, may be NULL; DEC_FP8_E4M3_ROWSCALE: fp32 row scales [vocab]).
+   All pointers are device memory the caller owns; inputs and weights 16-byte aligned.
+   Its scratch (step state, argmax partials, status) is a static device array of 64 KiB in
+   the library, which every GPU that loads the library keeps until the process exits; a call
+   needs about 256 * 5 + 32 * (SM count) bytes of it and returns DEC_ERR_CAPACITY beyond that.
+   The first call on a device looks up the array's device address, so make it before any
+   stream capture. Every call clears and reuses the same array: calls that overlap on the GPU
+   (other streams, other threads) race, so serialise them. Waits for the result
+   (synchronises the stream) and returns a device error if the kernel raised one.
+   m: 1..4; hidden a multiple of 64. */
+dec_status dec_lm_head_noalloc(int hidden, int vocab, dec_dtype dtype, int m, float rms_eps, const void* hidden_dev,
+                               const void* final_norm_dev, const void* w_values_dev, const void* w_scales_dev,
+                               float* logits_dev, int32_t* argmax_dev, void* cuda_stream);
+
 /* Text of the last error raised on the calling thread ("" if none). */
 const char* dec_last_error(void);
 

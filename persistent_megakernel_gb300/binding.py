@@ -36,7 +36,7 @@ DEC_MODE_PER_OP_GRAPH = 2
 # every symbol include/dec.h declares
 EXPORTS = ("dec_workspace_bytes", "dec_init", "dec_load_weights", "dec_set_kv_cache", "dec_step", "dec_generate",
            "dec_verify", "dec_debug_buffers", "dec_reset", "dec_sync", "dec_last_launch_count", "dec_last_error",
-           "dec_free", "dec_packed_bytes", "dec_pack", "dec_pack_pair", "dec_trace_buffer")
+           "dec_free", "dec_packed_bytes", "dec_pack", "dec_pack_pair", "dec_trace_buffer", "dec_lm_head_noalloc")
 
 
 class DecConfig(ctypes.Structure):
@@ -87,6 +87,7 @@ def lib():
             "dec_packed_bytes": (I, [I, I, I, ctypes.POINTER(SZ), ctypes.POINTER(SZ)]),
             "dec_pack": (I, [I, P, I, I, P, P]),
             "dec_pack_pair": (I, [I, P, P, I, I, P, P]),
+            "dec_lm_head_noalloc": (I, [I, I, I, I, ctypes.c_float, P, P, P, P, P, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -188,6 +189,14 @@ def dec_packed_bytes(dtype: int, rows: int, cols: int):
     v, s = ctypes.c_size_t(), ctypes.c_size_t()
     check(lib().dec_packed_bytes(dtype, rows, cols, ctypes.byref(v), ctypes.byref(s)))
     return v.value, s.value
+
+
+def dec_lm_head_noalloc(hidden: int, vocab: int, dtype: int, m: int, rms_eps: float, hidden_dev, final_norm_dev,
+                        w_values_dev, w_scales_dev, logits_dev, argmax_dev, stream) -> None:
+    """The LM head for callers that cannot allocate device memory (all buffers are the caller's;
+    the library's static scratch serves the kernel). Synchronises the stream."""
+    check(lib().dec_lm_head_noalloc(hidden, vocab, dtype, m, rms_eps, _p(hidden_dev), _p(final_norm_dev),
+                                    _p(w_values_dev), _p(w_scales_dev), _p(logits_dev), _p(argmax_dev), _p(stream)))
 
 
 def dec_pack(dtype: int, w_bf16, rows: int, cols: int, out_values, out_scales=None) -> None:

@@ -904,6 +904,116 @@ dec_status dec_sync(dec_ctx* c) {
 
 int dec_last_launch_count(dec_ctx* c) { return c ? c->last_launches : 0; }
 
+dec_status dec_lm_head_noalloc(int hidden, int vocab, dec_dtype dtype, int m, float rms_eps, const void* hidden_dev,
+                               const void* final_norm_dev, const void* w_values_dev, const void* w_scales_dev,
+                               float* logits_dev, int32_t* argmax_dev, void* cuda_stream) {
+  auto misaligned = [](const void* q) { return reinterpret_cast<uintptr_t>(q) % 16 != 0; };
+  if (hidden <= 0 || hidden % 64) return fail(DEC_ERR_SHAPE, "hidden must be a positive multiple of 64");
+  if (vocab <= 0) return fail(DEC_ERR_SHAPE, "vocab must be positive");
+  if (m < 1 || m > kMmax) return fail(DEC_ERR_SHAPE, "m must be 1..%d", kMmax);
+  if (dtype != DEC_BF16 && dtype != DEC_FP8_E4M3_ROWSCALE)
+    return fail(DEC_ERR_DTYPE, "dtype must be DEC_BF16 or DEC_FP8_E4M3_ROWSCALE");
+  if (!std::isfinite(rms_eps) || rms_eps < 0) return fail(DEC_ERR_INVALID_ARG, "rms_eps must be >= 0");
+  if (!hidden_dev || misaligned(hidden_dev)) return fail(DEC_ERR_INVALID_ARG, "hidden_dev null or not 16-byte aligned");
+  if (!w_values_dev || misaligned(w_values_dev)) return fail(DEC_ERR_INVALID_ARG, "w_values_dev null or not 16-byte aligned");
+  if (dtype == DEC_FP8_E4M3_ROWSCALE && (!w_scales_dev || misaligned(w_scales_dev)))
+    return fail(DEC_ERR_INVALID_ARG, "w_scales_dev null or not 16-byte aligned");
+  if (final_norm_dev && misaligned(final_norm_dev)) return fail(DEC_ERR_INVALID_ARG, "final_norm_dev not 16-byte aligned");
+  if (!logits_dev || !argmax_dev) return fail(DEC_ERR_INVALID_ARG, "logits_dev and argmax_dev are required");
+
+  int dev = 0, C = 0;
+  CUDA_TRY(cudaGetDevice(&dev));
+  CUDA_TRY(cudaDeviceGetAttribute(&C, cudaDevAttrMultiProcessorCount, dev));
+  // scratch: step state, status word, tickets, arrival counter, the op, per-CTA argmax partials
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align_up(o + bytes, 256);
+    return at;
+  };
+  const size_t off_state = take(sizeof(StepState)), off_status = take(sizeof(Status)), off_tickets = take(2 * 4),
+               off_ctr = take(4), off_op = take(sizeof(OpDesc)), off_val = take((size_t)C * kMmax * 4),
+               off_idx = take((size_t)C * kMmax * 4);
+  if (o > (size_t)kNoAllocScratchBytes)
+    return fail(DEC_ERR_CAPACITY, "the allocation-free LM head needs %zu bytes of scratch for %d SMs; it has %d", o, C,
+                kNoAllocScratchBytes);
+  void* scratch_ptr = nullptr;
+  CUDA_TRY(noalloc_scratch(&scratch_ptr));
+  uint8_t* scratch = static_cast<uint8_t*>(scratch_ptr);
+
+  // shared memory: the same sizing as a context holding only an LM head
+  const int rows_cta = (hidden + C - 1) / C + 16;
+  size_t act = std::max((size_t)m * hidden, (size_t)2 * kConsumerThreads);
+  act = std::max(act, (size_t)m * hidden + (size_t)2 * (rows_cta + 1) * m * kConsumerWarps);
+  act = align_up(act * 4, 256);
+  long long slot = ((long long)kSmemLimit - (long long)act - dec_megakernel_common_bytes()) / (kConsumerWarps * kStages);
+  slot = std::min<long long>(slot / 256 * 256, kMaxSlotBytes);
+  if (slot < 4096) return fail(DEC_ERR_SHAPE, "hidden %d needs more shared memory than a CTA has", hidden);
+
+  OpDesc h;
+  std::memset(&h, 0, sizeof(h));
+  h.type = OP_LMHEAD;
+  h.wtype = dtype == DEC_FP8_E4M3_ROWSCALE ? W_FP8 : W_BF16;
+  h.N = vocab;
+  h.K = hidden;
+  h.ticket = 0;
+  h.ctr = 0;
+  h.wait_ctr = -1;
+  h.wait_n = C;
+  h.aux_ctr = -1;
+  h.norm = final_norm_dev ? 1 : 0;
+  h.xsrc = X_HIDDEN_IN;
+  h.slot1 = -1;
+  h.gain = static_cast<const uint16_t*>(final_norm_dev);
+  h.w = w_values_dev;
+  h.ws = w_scales_dev;
+  h.logits = logits_dev;
+  tile_geometry(h.wtype, h.K, 0, (int)slot, m, h.R, h.Kc, h.unit);
+
+  StepState st;
+  std::memset(&st, 0, sizeof(st));
+  st.m = m;
+  st.hidden_in = hidden_dev;
+
+  KParams k;
+  std::memset(&k, 0, sizeof(k));
+  k.ops = reinterpret_cast<const OpDesc*>(scratch + off_op);
+  k.op_begin = 0;
+  k.op_end = k.n_ops = 1;
+  k.n_ctas = C;
+  k.H = hidden;
+  k.G = 1;
+  k.V = vocab;
+  k.Mmax = m;
+  k.ns_max = 1;
+  k.eps = rms_eps;
+  k.timeout_ns = 2000000000ull;
+  k.slot_bytes = (int)slot;
+  k.act_bytes = (int)act;
+  k.state = reinterpret_cast<StepState*>(scratch + off_state);
+  k.status = reinterpret_cast<Status*>(scratch + off_status);
+  k.tickets = reinterpret_cast<uint32_t*>(scratch + off_tickets);
+  k.ctr = reinterpret_cast<uint32_t*>(scratch + off_ctr);
+  k.am_val = reinterpret_cast<float*>(scratch + off_val);
+  k.am_idx = reinterpret_cast<int32_t*>(scratch + off_idx);
+  k.am_out = argmax_dev;
+  k.step_ticket = 1;
+
+  // the scratch keeps the previous call's contents: everything the kernel counts from starts at zero
+  cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+  CUDA_TRY(cudaMemsetAsync(scratch, 0, o, stream));
+  CUDA_TRY(cudaMemcpyAsync(scratch + off_op, &h, sizeof(h), cudaMemcpyHostToDevice, stream));
+  CUDA_TRY(cudaMemcpyAsync(scratch + off_state, &st, sizeof(st), cudaMemcpyHostToDevice, stream));
+  CUDA_TRY(dec_launch_megakernel(&k, 1, stream));
+  Status sw;
+  CUDA_TRY(cudaMemcpyAsync(&sw, scratch + off_status, sizeof(sw), cudaMemcpyDeviceToHost, stream));
+  CUDA_TRY(cudaStreamSynchronize(stream));
+  if (sw.code != 0)
+    return fail((dec_status)sw.code, "device wait timed out in the allocation-free LM head (cta %d, site %u)", sw.cta,
+                sw.where);
+  return DEC_OK;
+}
+
 void dec_free(dec_ctx* c) {
   if (!c) return;
   if (c->graph) cudaGraphExecDestroy(c->graph);

@@ -14,6 +14,7 @@
 // for the CTA's bulk copies in flight); a consumer waits for the count with one thread, then
 // loads the data and checks every word's tag, re-reading the rare word not yet visible.
 #pragma once
+#include <cuda_runtime.h>
 #include <stdint.h>
 
 namespace decimpl {
@@ -34,6 +35,7 @@ constexpr int kMaxRouteSlots = 1 + 8 * kMmax;    // shared + union of routed exp
 constexpr int kPart = 132;                       // attention partial: max, sum, 2 pad, output[128]
 constexpr int kMaxSlotBytes = 16384;             // one warp's ring slot at most (attention rows <= 32)
 constexpr int kSmemLimit = 232448;               // dynamic shared memory per CTA on sm_103a
+constexpr int kNoAllocScratchBytes = 64 * 1024;  // static scratch of the allocation-free LM head
 
 enum OpType : int32_t {
   OP_QKV = 0,           // a = RMSNorm(x); qkv = W_qkv a
@@ -136,5 +138,9 @@ constexpr int kTraceFields = 12;
 // compute done, slot released (5 stamps + pad per tile).
 constexpr int kTileLog = 1024;
 constexpr int kTileStamps = 6;
+
+// Device address of the allocation-free LM head's static scratch on the current device
+// (noalloc.cu); the first call on a device looks it up.
+cudaError_t noalloc_scratch(void** ptr);
 
 }  // namespace decimpl
