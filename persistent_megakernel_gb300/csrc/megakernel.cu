@@ -165,7 +165,7 @@ constexpr int kInflightBytes = DEC_INFLIGHT_KB * 1024;
 #define DEC_POLL_BACKOFF_NS 0  // pause before re-reading words whose tag is not current yet
 #endif
 #ifndef DEC_GATHER_U
-#define DEC_GATHER_U 8  // 4-word items each thread keeps in flight when loading an op's input
+#define DEC_GATHER_U 1  // 4-word items each thread keeps in flight when loading an op's input
 #endif
 constexpr int kGatherU = DEC_GATHER_U;
 
@@ -953,86 +953,73 @@ struct Consumer {
     }
   }
 
-  // act = RMSNorm(x_m) * gain (op.norm) or x_m for the M tokens, written in the quarter-plane
-  // layout of the op's weight type. Element group i = m*H/4 + k4 belongs to thread i mod
-  // threads in every CTA, so the sum of squares (thread partials in order, warp tree, warps in
-  // order) is the same everywhere. Returns this thread's polling verdict.
+  // act = x_m * gain (op.norm) or x_m for the M tokens, written in the quarter-plane layout of
+  // the op's weight type. RMSNorm's 1/rms is a scalar per token, so it is applied to the row
+  // sums in the epilogue instead (W (x g / rms) = (W (x g)) / rms): the prologue needs no
+  // barrier for it. Each thread sums the squares of the groups it loaded (group i = m*H/4 + k4
+  // belongs to thread i mod threads in every CTA), warps reduce by a fixed tree, and lane 0
+  // leaves the warp's partial in s.red[m * 8 + warp]; rstd() adds them in warp order, so every
+  // CTA computes the same value. Returns this thread's polling verdict.
   __device__ __forceinline__ bool norm_prologue(const OpDesc& op, int M, const uint2 (&gpre)[kGainPre], int oi) {
     const int H = p.H, H4 = H / 4, n4 = M * H4;
     const int cw = chunk_width(op.wtype), nvt = H / cw;
-    auto at = [&](int i) {
+    float ss[kMmax];
+#pragma unroll
+    for (int m = 0; m < kMmax; ++m) ss[m] = 0.f;
+    auto put = [&](int i, float4 x) {
       const int m = i / H4, k4 = i - m * H4;
-      return reinterpret_cast<float4*>(s.act + m * H + act_pos(4 * k4, cw, nvt));
+      if (op.norm) {
+        // gains: the first kGainPre vectors of this thread were loaded before the wait
+        const int u = (k4 - tid) / kConsumerThreads;
+        const uint2 g = (M == 1 && u < kGainPre)
+                            ? (u == 0 ? gpre[0] : (u == 1 ? gpre[1] : (u == 2 ? gpre[2] : gpre[3])))
+                            : __ldg(reinterpret_cast<const uint2*>(op.gain) + k4);
+#pragma unroll
+        for (int mm = 0; mm < kMmax; ++mm) {
+          if (mm == m) {
+            ss[mm] = fmaf(x.x, x.x, ss[mm]);
+            ss[mm] = fmaf(x.y, x.y, ss[mm]);
+            ss[mm] = fmaf(x.z, x.z, ss[mm]);
+            ss[mm] = fmaf(x.w, x.w, ss[mm]);
+          }
+        }
+        x.x *= bf16_lo(g.x);
+        x.y *= bf16_hi(g.x);
+        x.z *= bf16_lo(g.y);
+        x.w *= bf16_hi(g.y);
+      }
+      *reinterpret_cast<float4*>(s.act + m * H + act_pos(4 * k4, cw, nvt)) = x;
     };
     bool ok = true;
     if (op.xsrc == X_F32) {
       ok = gather<kGatherU, 4>(
           n4, [&](int i) { return x_tagged(op, i / H4) + 4 * (i % H4); },
-          [&](int i, const float (&v)[4]) { *at(i) = make_float4(v[0], v[1], v[2], v[3]); }, oi, 7);
+          [&](int i, const float (&v)[4]) { put(i, make_float4(v[0], v[1], v[2], v[3])); }, oi, 7);
       if (tid == 0) TRACE(p, oi, 8, gtimer());
     } else {
       for (int i = tid; i < n4; i += kConsumerThreads) {
         const uint2 u = __ldg(reinterpret_cast<const uint2*>(x_bf16(op, i / H4)) + i % H4);
-        *at(i) = make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
+        put(i, make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y)));
       }
     }
     if (op.norm) {
-      // every thread sums the squares of the groups it polled itself (token m's groups come in
-      // increasing i), so no barrier is needed before the reduction
-      float ss[kMmax], rstd[kMmax];
-      int i = tid;
 #pragma unroll
       for (int m = 0; m < kMmax; ++m) {
-        float acc = 0.f;
-        if (m < M)
-          for (; i < (m + 1) * H4; i += kConsumerThreads) {
-            const float4 x = *at(i);
-            acc = fmaf(x.x, x.x, acc);
-            acc = fmaf(x.y, x.y, acc);
-            acc = fmaf(x.z, x.z, acc);
-            acc = fmaf(x.w, x.w, acc);
-          }
+        float acc = ss[m];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        ss[m] = acc;
         if (lane == 0) s.red[m * 8 + warp] = acc;
       }
-      consumer_sync();
-#pragma unroll
-      for (int m = 0; m < kMmax; ++m) {
-        float tot = 0.f;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) tot += s.red[m * 8 + w];
-        rstd[m] = 1.0f / sqrtf(tot / (float)H + p.eps);
-      }
-      (void)ss;
-      auto scale = [&](int i, uint2 g, float r) {
-        float4* d = at(i);
-        float4 v = *d;
-        v.x = v.x * r * bf16_lo(g.x);
-        v.y = v.y * r * bf16_hi(g.x);
-        v.z = v.z * r * bf16_lo(g.y);
-        v.w = v.w * r * bf16_hi(g.y);
-        *d = v;
-      };
-      if (M == 1) {
-#pragma unroll
-        for (int u = 0; u < kGainPre; ++u) {
-          const int k4 = tid + u * kConsumerThreads;
-          if (k4 < H4) scale(k4, gpre[u], rstd[0]);
-        }
-        for (int k4 = tid + kGainPre * kConsumerThreads; k4 < H4; k4 += kConsumerThreads)
-          scale(k4, __ldg(reinterpret_cast<const uint2*>(op.gain) + k4), rstd[0]);
-      } else {
-        for (int j = tid; j < n4; j += kConsumerThreads) {
-          const int m = j / H4;
-          const float r = m == 0 ? rstd[0] : (m == 1 ? rstd[1] : (m == 2 ? rstd[2] : rstd[3]));
-          scale(j, __ldg(reinterpret_cast<const uint2*>(op.gain) + (j - m * H4)), r);
-        }
-      }
     }
-    consumer_sync();
     return ok;
+  }
+
+  // 1/rms of token m for ops whose prologue was norm_prologue (after the prologue's barrier).
+  __device__ __forceinline__ float rstd(int m) const {
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) tot += s.red[m * 8 + w];
+    return 1.0f / sqrtf(tot / (float)p.H + p.eps);
   }
 
   // dst = M rows of K tagged words polled from global (row stride src_stride words), in the
@@ -1177,6 +1164,8 @@ struct Consumer {
     Tile t;
     bool ok = true;
     const int i = lane / MT, m = lane % MT;
+    // the RMSNorm scale of lane's token (norm ops), applied to its row sums
+    const float rs = op.norm ? rstd(m < M ? m : 0) : 1.f;
     static_assert(NI == 0 || MT == 1, "register activations serve one token");
     ActRegs<WT, (NI > 0 ? NI : 1)> AR;
     if constexpr (NI > 0) act_regs_load(AR, s.act, op.K, 0, op.K, lane);
@@ -1194,7 +1183,7 @@ struct Consumer {
         warp_gemv<WT, MT, NR>(slot, t.nr, t.kn, t.kc, actp, op.K, M, A, lane);
       release(eb);
       if (!t.last_k) continue;
-      const float v = warp_rowsums<NR, MT>(A, t.nr, lane);
+      const float v = warp_rowsums<NR, MT>(A, t.nr, lane) * rs;
       acc_zero(A);
       const bool mine = lane < t.nr * MT && m < M;
       switch (op.type) {
@@ -1288,7 +1277,7 @@ struct Consumer {
     auto rowsum = [&](int r, int m) {
       float v = 0.f;
       for (int w = 0; w < kConsumerWarps; ++w) v += parts[(w * rows + r) * M + m];
-      return v;
+      return op.norm ? v * rstd(m) : v;
     };
     if (op.type == OP_GATEUP) {
       for (int t = tid; t < (rows / 2) * M; t += kConsumerThreads) {
