@@ -42,14 +42,17 @@ def peaks():
     return 6800.0, "fallback"
 
 
-def dist_setup(n_gpus):
+def dist_setup(n_gpus, backend: str = "nccl"):
+    """Rank, world size and local rank; one replica per GPU (torchrun env). The timing
+    reductions below are the only collectives: the decode path itself has none."""
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     if ws > 1:
-        import torch
         import torch.distributed as dist
         local = int(os.environ.get("LOCAL_RANK", "0"))
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
+        if backend == "nccl":
+            import torch
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
         return dist.get_rank(), ws, local
     return 0, 1, 0
 
@@ -65,9 +68,16 @@ def max_over_ranks(v: float, ws: int) -> float:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, secs: float, ws: int) -> float:
+    """Units all ranks processed over the slowest rank's time (weak scaling: every replica
+    runs the same per-GPU work)."""
+    return ws * units_per_rank / max_over_ranks(secs, ws)
 
 
 class Clocks:
@@ -269,7 +279,7 @@ def main():
     barrier(ws)
     clk = clocks.stop()
     secs_max = max_over_ranks(secs, ws)
-    value = ws * args.steps / secs_max
+    value = whole_job_rate(args.steps, secs, ws)
 
     # algorithmic bytes per step averaged over the positions the timed steps used
     poss = [pos0 + (i % CHAIN) for i in range(args.steps)]
@@ -287,8 +297,7 @@ def main():
     for i in range(K2):
         tok = B.dec_step(dec.ctx, tok, None, pos0 + i, None, True)
     e2e_secs = time.perf_counter() - t0
-    e2e_secs = max_over_ranks(e2e_secs, ws)
-    e2e = {"value": ws * K2 / e2e_secs, "unit": "tokens/s", "h2d_bytes_per_step": 60, "d2h_bytes_per_step": 36,
+    e2e = {"value": whole_job_rate(K2, e2e_secs, ws), "unit": "tokens/s", "h2d_bytes_per_step": 60, "d2h_bytes_per_step": 36,
            "steps": K2, "note": "dec_step per token: token and position copied in, argmax and status copied out"}
 
     compare = None
