@@ -158,6 +158,9 @@ __device__ __noinline__ bool wait_counter_slow(const KParams& p, const uint32_t*
 #define DEC_INFLIGHT_KB 256  // bytes of weight / KV copies one SM may keep in flight, in KiB
 #endif
 constexpr int kInflightBytes = DEC_INFLIGHT_KB * 1024;
+#ifndef DEC_POLL_DATA
+#define DEC_POLL_DATA 1  // 1: no arrival counts: consumers poll the tagged inputs directly
+#endif
 #ifndef DEC_ORDERED_ARRIVALS
 #define DEC_ORDERED_ARRIVALS 0  // 1: release/acquire arrivals (data visible when the count is)
 #endif
@@ -196,6 +199,9 @@ __device__ __noinline__ bool poll_item_slow(const KParams& p, const uint64_t* sr
       for (int k = 0; k < W; ++k) out[k] = value_of(w[k]);
       return true;
     }
+#if DEC_POLL_BACKOFF_NS > 0
+    __nanosleep(DEC_POLL_BACKOFF_NS);
+#endif
     if ((it & 7) == 0) {
       if (aborted(p)) return false;
       if (gtimer() - t0 > p.timeout_ns) {
@@ -837,6 +843,9 @@ struct Consumer {
   // Wait until counter c has n arrivals in this step. One thread spins; the others wait at the
   // barrier. The data behind the count is then read with its tags checked (gather).
   __device__ bool wait_counter(int c, int n, int oi, uint32_t where) {
+#if DEC_POLL_DATA
+    return true;  // the data is polled directly (its tags decide)
+#endif
     bool ok = true;
     if (tid == 0) {
       const uint32_t target = (epoch + 1u) * (uint32_t)n;
@@ -849,13 +858,16 @@ struct Consumer {
     return consumer_all(ok);
   }
 
-  // This CTA has written its share of what counter c announces.
+  // This CTA has written its share of what counter c announces (and its threads are done with
+  // the op: the barrier also guards the shared op copy).
   __device__ void arrive(int c) {
     consumer_sync();  // every warp's stores are issued
+#if !DEC_POLL_DATA
 #if DEC_ORDERED_ARRIVALS
     if (tid == 0) red_release(p.ctr + c, 1u);
 #else
     if (tid == 0) red_relaxed(p.ctr + c, 1u);
+#endif
 #endif
   }
 
