@@ -16,6 +16,10 @@
 
 using namespace decimpl;
 
+#ifndef DEC_ATTN_SPLIT_DIV
+#define DEC_ATTN_SPLIT_DIV 1
+#endif
+
 extern "C" cudaError_t dec_launch_megakernel(const KParams* kp, int cooperative, cudaStream_t stream);
 extern "C" int dec_megakernel_common_bytes(void);
 
@@ -164,7 +168,8 @@ bool compute_layout(const dec_config* c, Layout& L, std::string& why) {
   const int qkv_rows = c->n_q ? (c->n_q + 2 * c->n_kv) * kHeadDim : 0;
   L.n_ctas = C;
   L.n_ops = count_ops(c);
-  L.ns_max = c->n_q ? std::max(1, C / c->n_kv) : 1;
+  // attention splits per kv head: every CTA takes one split (fewer, longer splits: knob)
+  L.ns_max = c->n_q ? std::max(1, C / c->n_kv / DEC_ATTN_SPLIT_DIV) : 1;
   L.n_tickets = 2;  // LM-head argmax, step end
 
   // shared-memory scratch ("act") the largest op needs, in floats

@@ -677,6 +677,7 @@ __device__ __forceinline__ AttnScratch attn_scratch(const KParams& p, const Smem
   f = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(f) + 15) & ~uintptr_t(15));
   a.ml = reinterpret_cast<float2*>(f);
   f += 2 * MG * ns;
+  f = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(f) + 15) & ~uintptr_t(15));  // float4 rows
   a.raw = f;
   return a;
 }
