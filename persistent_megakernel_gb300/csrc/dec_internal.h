@@ -9,10 +9,10 @@
 // already in flight while the previous op is still being finished elsewhere (the
 // multiprogramming argument of the Muse Spark Open megakernel article, section "the
 // baseline nobody benchmarked", and its weight-prefetch ring, section "three bills").
-// Activations travel as tagged words (value + step tag). When a CTA has written its share of
-// an op it bumps the op's arrival counter with a relaxed atomic (no fence: a fence would wait
-// for the CTA's bulk copies in flight); a consumer waits for the count with one thread, then
-// loads the data and checks every word's tag, re-reading the rare word not yet visible.
+// Activations travel as tagged words (value + step tag): a consumer reads the words it needs
+// and re-reads any whose tag is not the current step's yet, so a writer never executes a fence
+// (a fence would wait for the CTA's bulk copies in flight). Per-op arrival counters (relaxed
+// atomics) remain as a build option that gates the reads on a count instead.
 #pragma once
 #include <cuda_runtime.h>
 #include <stdint.h>

@@ -171,6 +171,10 @@ constexpr int kInflightBytes = DEC_INFLIGHT_KB * 1024;
 #define DEC_GATHER_U 1  // 4-word items each thread keeps in flight when loading an op's input
 #endif
 constexpr int kGatherU = DEC_GATHER_U;
+#ifndef DEC_COPY_U
+#define DEC_COPY_U 1  // the same for the o-proj / down-projection inputs (up to 6912 words a token)
+#endif
+constexpr int kCopyU = DEC_COPY_U;
 
 // One item of W tagged words (W = 2 or 4: 16-byte aligned).
 template <int W>
@@ -841,8 +845,10 @@ struct Consumer {
     return s.flags[kFlagTicket] != 0;
   }
 
-  // Wait until counter c has n arrivals in this step. One thread spins; the others wait at the
-  // barrier. The data behind the count is then read with its tags checked (gather).
+  // Wait until counter c has n arrivals in this step (builds with DEC_POLL_DATA=0). One thread
+  // spins; the others wait at the barrier; the data behind the count is then read with its tags
+  // checked (gather). By default the inputs are polled directly and this returns at once: a
+  // ready input then costs one round trip to L2 instead of two.
   __device__ bool wait_counter(int c, int n, int oi, uint32_t where) {
 #if DEC_POLL_DATA
     return true;  // the data is polled directly (its tags decide)
@@ -1039,7 +1045,7 @@ struct Consumer {
   // quarter-plane layout of chunk width cw.
   __device__ __forceinline__ bool copy_act(float* dst, const uint64_t* src, int M, int K, int src_stride, int cw, int oi) {
     const int K4 = K / 4, nvt = K / cw;
-    return gather<kGatherU, 4>(
+    return gather<kCopyU, 4>(
         M * K4, [&](int i) { return src + (size_t)(i / K4) * src_stride + 4 * (i % K4); },
         [&](int i, const float (&v)[4]) {
           *reinterpret_cast<float4*>(dst + (i / K4) * K + act_pos(4 * (i % K4), cw, nvt)) =
