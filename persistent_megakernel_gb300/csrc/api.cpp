@@ -179,12 +179,9 @@ bool compute_layout(const dec_config* c, Layout& L, std::string& why) {
   if (c->n_q) {
     const size_t MG = (size_t)M * G;
     act = std::max(act, (size_t)M * c->n_q * kHeadDim + (size_t)rows_cta * M * (1 + kConsumerWarps));
-    // queries, per-warp scores (<= 32 rows) reused for the merge's output slices, per-warp merge
-    // state, own keys/values, merge weights, the splits' (max, sum), the polled q/k/v rows
-    const size_t prods = ((MG * 32 + L.ns_max - 1) / L.ns_max + 1) * L.ns_max * 4;
-    act = std::max(act, MG * 128 + std::max((size_t)kConsumerWarps * G * 32, prods) + 4 +
-                            (size_t)kConsumerWarps * G * kPart + 2 * kMmax * 128 / 2 + MG * L.ns_max + 4 +
-                            2 * MG * L.ns_max + (size_t)M * (G + 2) * 128 + 64);
+    // the attention scratch the kernel carves (at most 32 KV rows per ring slot)
+    (void)MG;
+    act = std::max(act, (size_t)attn_layout(M, G, kMaxSlotBytes / 512, L.ns_max).end);
   }
   if (c->ffn) act = std::max(act, (size_t)M * c->ffn + (size_t)rows_cta * M * (1 + kConsumerWarps));
   act = std::max(act, (size_t)M * H + (size_t)2 * (rows_cta + 1) * M * kConsumerWarps);  // column-split partials

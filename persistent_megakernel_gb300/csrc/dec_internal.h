@@ -139,6 +139,35 @@ constexpr int kTraceFields = 12;
 constexpr int kTileLog = 1024;
 constexpr int kTileStamps = 6;
 
+#ifdef __CUDACC__
+#define DEC_HD __host__ __device__
+#else
+#define DEC_HD
+#endif
+
+// Attention scratch inside a CTA's activation area, in floats from its (256-byte aligned) start;
+// the kernel carves it and the host sizes the area with the same function. P: KV rows per
+// ring slot; ns: splits per kv head.
+struct AttnLayout {
+  int q, sc, mg, kvn, cw, ml, raw, end;
+};
+
+DEC_HD inline AttnLayout attn_layout(int M, int G, int P, int ns) {
+  auto up4 = [](int f) { return (f + 3) & ~3; };  // 16-byte boundary
+  const int MG = M * G;
+  const int prods = ((MG * 32 + ns - 1) / ns + 1) * ns * 4;  // the merge's output slices of every split
+  AttnLayout l;
+  l.q = 0;                                                      // [M*G][128] rotated queries
+  l.sc = l.q + MG * 128;                                        // per-warp scores / merge slices
+  l.mg = up4(l.sc + (kConsumerWarps * G * P > prods ? kConsumerWarps * G * P : prods));
+  l.kvn = l.mg + kConsumerWarps * G * kPart;                    // per-warp split states
+  l.cw = l.kvn + kMmax * 128;                                   // own keys / values (bf16 [2][M][128])
+  l.ml = up4(l.cw + MG * ns);                                   // merge weights
+  l.raw = up4(l.ml + 2 * MG * ns);                              // splits' (max, sum)
+  l.end = l.raw + M * (G + 2) * 128;                            // polled q / k / v rows
+  return l;
+}
+
 // Device address of the allocation-free LM head's static scratch on the current device
 // (noalloc.cu); the first call on a device looks it up.
 cudaError_t noalloc_scratch(void** ptr);

@@ -661,28 +661,15 @@ struct AttnScratch {
 };
 
 __device__ __forceinline__ AttnScratch attn_scratch(const KParams& p, const Smem& s, int M, int P) {
+  const AttnLayout l = attn_layout(M, p.G, P, p.ns_max);
   AttnScratch a;
-  const int MG = M * p.G, ns = p.ns_max;
-  float* f = s.act;
-  a.q = f;
-  f += MG * 128;
-  {
-    const int prods = ((MG * 32 + ns - 1) / ns + 1) * ns * 4;  // merge: output slices of every split
-    a.sc = f;
-    f += max(kConsumerWarps * p.G * P, prods);
-    f = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(f) + 15) & ~uintptr_t(15));
-  }
-  a.mg = f;
-  f += kConsumerWarps * p.G * kPart;
-  a.kvn = reinterpret_cast<uint16_t*>(f);
-  f += 2 * kMmax * 128 / 2;
-  a.cw = f;
-  f += MG * ns;
-  f = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(f) + 15) & ~uintptr_t(15));
-  a.ml = reinterpret_cast<float2*>(f);
-  f += 2 * MG * ns;
-  f = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(f) + 15) & ~uintptr_t(15));  // float4 rows
-  a.raw = f;
+  a.q = s.act + l.q;
+  a.sc = s.act + l.sc;
+  a.mg = s.act + l.mg;
+  a.kvn = reinterpret_cast<uint16_t*>(s.act + l.kvn);
+  a.cw = s.act + l.cw;
+  a.ml = reinterpret_cast<float2*>(s.act + l.ml);
+  a.raw = s.act + l.raw;
   return a;
 }
 
