@@ -176,6 +176,14 @@ dec_status dec_reset(dec_ctx* ctx);
 /* Wait for the context's stream; returns a sticky device error if one was raised. */
 dec_status dec_sync(dec_ctx* ctx);
 
+/* Failure injection for tests (host side only): the next call of a DEC_MODE_PER_OP context
+   skips launching op `op` of the step (0-based, in list order; -1 cancels), so its outputs are
+   never written. The op that reads them waits spin_timeout_ns, records the failure in the status
+   word and raises the abort flag; every later wait of the step returns at once. The call
+   returns DEC_ERR_TIMEOUT (sticky until dec_reset) and the GPU context stays usable.
+   DEC_ERR_STATE in other modes; DEC_ERR_INVALID_ARG for an op outside the step. */
+dec_status dec_debug_drop_op(dec_ctx* ctx, int op);
+
 /* Number of kernel launches the last dec_step / dec_verify issued (1 in persistent mode). */
 int dec_last_launch_count(dec_ctx* ctx);
 

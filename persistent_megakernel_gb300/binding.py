@@ -36,7 +36,7 @@ DEC_MODE_PER_OP_GRAPH = 2
 # every symbol include/dec.h declares
 EXPORTS = ("dec_workspace_bytes", "dec_init", "dec_load_weights", "dec_set_kv_cache", "dec_step", "dec_generate",
            "dec_verify", "dec_debug_buffers", "dec_reset", "dec_sync", "dec_last_launch_count", "dec_last_error",
-           "dec_free", "dec_packed_bytes", "dec_pack", "dec_pack_pair", "dec_trace_buffer", "dec_lm_head_noalloc")
+           "dec_free", "dec_packed_bytes", "dec_pack", "dec_pack_pair", "dec_trace_buffer", "dec_lm_head_noalloc", "dec_debug_drop_op")
 
 
 class DecConfig(ctypes.Structure):
@@ -82,6 +82,7 @@ def lib():
             "dec_reset": (I, [P]),
             "dec_sync": (I, [P]),
             "dec_last_launch_count": (I, [P]),
+            "dec_debug_drop_op": (I, [P, I]),
             "dec_last_error": (ctypes.c_char_p, []),
             "dec_free": (None, [P]),
             "dec_packed_bytes": (I, [I, I, I, ctypes.POINTER(SZ), ctypes.POINTER(SZ)]),
@@ -175,6 +176,10 @@ def dec_reset(ctx: int) -> None:
 
 def dec_sync(ctx: int) -> None:
     check(lib().dec_sync(ctx))
+
+
+def dec_debug_drop_op(ctx: int, op: int) -> None:
+    check(lib().dec_debug_drop_op(ctx, op))
 
 
 def dec_last_launch_count(ctx: int) -> int:

@@ -264,6 +264,7 @@ struct dec_ctx {
   dec_status sticky_code = DEC_OK;
   cudaGraphExec_t graph = nullptr;
   int last_launches = 0;
+  int drop_op = -1;  // failure injection: the next per-op call skips launching this op
 };
 
 namespace {
@@ -601,13 +602,18 @@ dec_status launch_step(dec_ctx* c) {
     c->last_launches = k.n_ops;
     return DEC_OK;
   }
+  const int drop = c->drop_op;
+  c->drop_op = -1;
+  int launched = 0;
   for (int i = 0; i < k.n_ops; ++i) {
+    if (i == drop) continue;  // injected failure: this op's outputs are never written
     KParams ki = k;
     ki.op_begin = i;
     ki.op_end = i + 1;
     CUDA_TRY(dec_launch_megakernel(&ki, 0, c->stream));
+    ++launched;
   }
-  c->last_launches = k.n_ops;
+  c->last_launches = launched;
   return DEC_OK;
 }
 
@@ -905,6 +911,15 @@ dec_status dec_sync(dec_ctx* c) {
 }
 
 int dec_last_launch_count(dec_ctx* c) { return c ? c->last_launches : 0; }
+
+dec_status dec_debug_drop_op(dec_ctx* c, int op) {
+  if (!c) return fail(DEC_ERR_INVALID_ARG, "null context");
+  if (c->cfg.mode != DEC_MODE_PER_OP) return fail(DEC_ERR_STATE, "ops can be dropped only in DEC_MODE_PER_OP");
+  if (op < -1 || op >= count_ops(&c->cfg)) return fail(DEC_ERR_INVALID_ARG, "op %d outside the step's %d ops", op,
+                                                       count_ops(&c->cfg));
+  c->drop_op = op;
+  return DEC_OK;
+}
 
 dec_status dec_lm_head_noalloc(int hidden, int vocab, dec_dtype dtype, int m, float rms_eps, const void* hidden_dev,
                                const void* final_norm_dev, const void* w_values_dev, const void* w_scales_dev,

@@ -123,3 +123,28 @@ def test_pair_packer_interleaves_rows(B):
     out = np.empty(12 * 64, np.uint16)
     B.dec_pack_pair(B.DEC_BF16, a, b, 6, 64, out, None)
     assert np.array_equal(out.reshape(12, 64), inter)
+
+
+def test_drop_op_only_in_per_op_mode():
+    """The failure-injection hook refuses persistent contexts and ops outside the step (no GPU
+    work: the checks come before any launch)."""
+    from persistent_megakernel_gb300 import binding as B
+    from persistent_megakernel_gb300.model import make_config
+    from synth.configs import ModelShape
+    import torch
+    s = ModelShape("t", n_layers=1, hidden=256, n_q=4, n_kv=2, ffn=352, vocab=1000, kv_prefill=8)
+    for mode, op, code in (("persistent", 0, B.DEC_ERR_STATE), ("per_op", 99, B.DEC_ERR_INVALID_ARG)):
+        cfg = make_config(s, 16, 1, mode, num_ctas=3)
+        n = B.dec_workspace_bytes(cfg)
+        ws = torch.zeros(n + 256, dtype=torch.uint8)
+        off = (-ws.data_ptr()) % 256
+        try:
+            ctx = B.dec_init(cfg, None, ws[off:off + n])
+        except B.DecError:
+            pytest.skip("dec_init needs a CUDA runtime")
+        try:
+            with pytest.raises(B.DecError) as e:
+                B.dec_debug_drop_op(ctx, op)
+            assert e.value.code == code
+        finally:
+            B.dec_free(ctx)
