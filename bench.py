@@ -161,23 +161,29 @@ def build_workload(seed: int, layers: int = 0):
 
 
 def cpu_baseline(s, layers, head, kv, seed):
-    """The oracle as it stands, one full decode step (28 layers + LM head) at position 4096."""
+    """The oracle as it stands: full decode steps (28 layers + LM head, weights decoded to fp64
+    in every step) at positions 4096, 4097, ... until about 10 s of CPU work (at most 6 steps)."""
     import synth
     from oracle.model import OracleModel
-    orc = OracleModel(s, layers, head, kv=kv, capacity=s.kv_prefill + 2)
+    orc = OracleModel(s, layers, head, kv=kv, capacity=s.kv_prefill + 8)
     tok = synth.start_token(seed, s.vocab)
-    t0 = time.perf_counter()
-    orc.step_token(tok, s.kv_prefill)
-    dt = time.perf_counter() - t0
+    n, t0 = 0, time.perf_counter()
+    while n < 6 and (n == 0 or time.perf_counter() - t0 < 10.0):
+        tok = orc.step_token(tok, s.kv_prefill + n)["token"]
+        n += 1
+    dt = (time.perf_counter() - t0) / n
     cores = len(os.sched_getaffinity(0))
     return {"value": 1.0 / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"one full decode step (28 layers + LM head, pos 4096) of the fp64 numpy oracle: {dt:.2f} s"}
+            "sample": f"{n} full greedy decode steps (28 layers + LM head, pos 4096..) of the fp64 numpy oracle: "
+                      f"{dt:.2f} s per step"}
 
 
 def run_reference(args):
     """Reference arm: the CPU oracle on the same workload; each step = one decoder layer of one
-    token (attention + FFN of layer i mod 28 at position 4096 + i mod 256), throughput scaled
-    by that layer's share of the token's algorithmic bytes."""
+    token (attention + FFN of layer i mod 4 at position 4096 + i mod 256; the 28 layers have the
+    same shape), throughput scaled by that layer's share of the token's algorithmic bytes. The
+    4 layers' weights are decoded to fp64 once, before the warm-up, so a run of K steps stays
+    within minutes and a few GB of host memory."""
     if int(os.environ.get("RANK", "0")) != 0:
         return  # the oracle runs once, on rank 0; other ranks exit without work
     import synth
@@ -189,11 +195,15 @@ def run_reference(args):
     per_token = R.algorithmic_bytes(s, s.kv_prefill)
     layer_bytes = R.layer_weight_bytes(s) + R.kv_bytes(s, s.kv_prefill) / s.n_layers
 
+    ref_layers = 4
+
     def one(i):
-        l, pos = i % s.n_layers, s.kv_prefill + (i % CHAIN)
+        l, pos = i % ref_layers, s.kv_prefill + (i % CHAIN)
         y = orc.attention_block(l, x, pos)
         orc.ffn_block(l, y, {})
 
+    for i in range(ref_layers):  # decode the sampled layers' weights (setup, like loading)
+        one(i)
     for i in range(args.warmup):
         one(i)
     t0 = time.perf_counter()
@@ -209,7 +219,8 @@ def run_reference(args):
         "config": {"workload": f"dense_2b: {s.n_layers} layers, hidden 2560, GQA 20/4 x 128, FFN 6912, vocab 32768, "
                                "KV prefill 4096, batch 1", "step": "one decoder layer of one token"},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                         "sample": "one decoder layer (attention + FFN) per step, fp64 numpy, weights pre-decoded"},
+                         "sample": "one decoder layer (attention + FFN, layers 0-3 in turn) per step, fp64 numpy, "
+                                   "weights decoded once before timing"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }))
 
