@@ -302,9 +302,10 @@ void build_ops(dec_ctx* c) {
   int ticket = 0;
   // x of the next block: the call's input first, then the hidden-stream entry last written
   int xsrc = g.embedding ? X_EMBED : X_HIDDEN_IN, x_idx = 0;
-  // every op announces its completion on its own counter; an op waits for the counter of the op
-  // that produced its newest input (ops run in list order in every CTA, so older inputs are
-  // complete too)
+  // dependencies for builds that gate reads on arrival counts (DEC_POLL_DATA=0; by default the
+  // kernel polls the tagged inputs directly): every op announces its completion on its own
+  // counter, and an op waits for the counter of the op that produced its newest input (ops run
+  // in list order in every CTA, so older inputs are complete too)
   int prev = -1;
   auto blank = [&](int type) {
     OpDesc o;
