@@ -148,3 +148,26 @@ def test_drop_op_only_in_per_op_mode():
             assert e.value.code == code
         finally:
             B.dec_free(ctx)
+
+
+@pytest.mark.parametrize("hidden,n_q,n_kv,ffn,experts", [(1024, 8, 2, 2816, 0), (2560, 20, 4, 6912, 0),
+                                                          (2560, 20, 4, 0, 512), (4096, 32, 8, 11008, 0),
+                                                          (256, 4, 2, 352, 0)])
+@pytest.mark.parametrize("m", [1, 2, 4])
+@pytest.mark.parametrize("ctas", [1, 3, 152, 304])
+def test_workspace_sizing_sweep(hidden, n_q, n_kv, ffn, experts, m, ctas):
+    """Host-side layout for a sweep of shapes, windows and grid sizes: either a workspace size
+    or a clear shape error (no device needed when the grid size is given)."""
+    from persistent_megakernel_gb300 import binding as B
+    from persistent_megakernel_gb300.model import make_config
+    from synth.configs import ModelShape
+    s = ModelShape("sweep", n_layers=2, hidden=hidden, n_q=n_q, n_kv=n_kv, ffn=ffn, n_experts=experts,
+                   top_k=8 if experts else 0, moe_inter=768 if experts else 0, n_shared=1 if experts else 0,
+                   vocab=32000, kv_prefill=128, embedding=True)
+    cfg = make_config(s, 256, m, "persistent", num_ctas=ctas)
+    n = B.dec_workspace_bytes(cfg)
+    if n == 0:
+        assert "shared memory" in B.dec_last_error(), B.dec_last_error()
+    else:
+        # at least the tagged hidden stream and the logits
+        assert n >= (2 * s.n_layers + 1) * m * hidden * 8 + m * s.vocab * 4
