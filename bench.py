@@ -8,6 +8,10 @@ o-proj / SwiGLU FFN, final norm, LM head, argmax) -- one launch of the persisten
 megakernel. Steps run in chains of 256 (positions 4096..4351, the workload's 256 greedy
 steps), repeated until K steps are timed.
 
+``--workload moe_stack`` times the 42-layer MoE stack instead (GQA 20/4 over a 32768-position
+cache, MoE of 512 MXFP4 experts top-8 + 1 shared, FP8 LM head 157184 x 2560, 512 greedy steps
+per chain, positions 32768..33279); its 67 GB of experts are drawn and packed on the device.
+
 Prints ONE JSON line (rank 0). Multi-GPU runs are replicas: every rank decodes its own
 request on its own GPU with no communication on the data path; value = all ranks' tokens /
 the slowest rank's time (weak scaling). ``--impl reference`` times the CPU oracle instead.
@@ -160,6 +164,48 @@ def build_workload(seed: int, layers: int = 0):
     return s, layers, head, kv
 
 
+WORKLOADS = {
+    "dense_2b": "dense_2b: {L} layers, hidden 2560, GQA 20/4 x 128, SwiGLU 6912, vocab 32768, KV prefill 4096, "
+                "batch 1, greedy, chains of 256 steps (pos 4096-4351)",
+    "moe_stack": "moe_stack: {L} layers, hidden 2560, GQA 20/4 x 128, MoE 512 experts top-8 + 1 shared "
+                 "(intermediate 768, MXFP4), FP8 LM head 157184 x 2560, KV prefill 32768, batch 1, greedy, "
+                 "chains of 512 steps (pos 32768-33279)",
+}
+
+
+def workload_shape(name: str, layers: int = 0):
+    import synth
+    s = synth.dense_2b_shape() if name == "dense_2b" else synth.moe_stack_shape()
+    return s.with_(n_layers=layers) if layers else s
+
+
+def cpu_baseline_layer(s, seed):
+    """The oracle on one decoder layer of one token of a large workload (attention over the
+    cache + FFN of layer 0, its weights decoded as the oracle does in every step), repeated until
+    about 10 s of CPU work; tokens/s scaled by the layer's share of the token's bytes."""
+    import synth
+    from synth import model as sm
+    from oracle.model import OracleModel
+    from persistent_megakernel_gb300 import roofline as R
+    s1 = s.with_(n_layers=1)
+    experts = (lambda l, e: sm.expert_weights(s, seed, 0, e)) if s.moe else None
+    orc = OracleModel(s1, [sm.layer_weights(s, seed, 0)], sm.head_weights(s, seed), experts=experts,
+                      kv=[sm.kv_prefill(s, seed, 0)], capacity=s.kv_prefill + 8)
+    x = orc.embed(synth.start_token(seed, s.vocab))
+    n, t0 = 0, time.perf_counter()
+    while n < 6 and (n == 0 or time.perf_counter() - t0 < 10.0):
+        y = orc.attention_block(0, x, s.kv_prefill)
+        orc.ffn_block(0, y, {})
+        n += 1
+    dt = (time.perf_counter() - t0) / n
+    share = (R.layer_weight_bytes(s) + R.kv_bytes(s, s.kv_prefill) / s.n_layers) / R.algorithmic_bytes(s, s.kv_prefill)
+    cores = len(os.sched_getaffinity(0))
+    return {"value": share / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} x one decoder layer (attention over {s.kv_prefill + 1} positions + FFN, weights and "
+                      f"experts decoded per step) of one token, fp64 numpy: {dt:.2f} s per layer, scaled by the "
+                      f"layer's share {share:.4f} of the token's bytes"}
+
+
 def cpu_baseline(s, layers, head, kv, seed):
     """The oracle as it stands: full decode steps (28 layers + LM head, weights decoded to fp64
     in every step) at positions 4096, 4097, ... until about 10 s of CPU work (at most 6 steps)."""
@@ -180,25 +226,33 @@ def cpu_baseline(s, layers, head, kv, seed):
 
 def run_reference(args):
     """Reference arm: the CPU oracle on the same workload; each step = one decoder layer of one
-    token (attention + FFN of layer i mod 4 at position 4096 + i mod 256; the 28 layers have the
-    same shape), throughput scaled by that layer's share of the token's algorithmic bytes. The
-    4 layers' weights are decoded to fp64 once, before the warm-up, so a run of K steps stays
-    within minutes and a few GB of host memory."""
+    token (dense 2B: attention + FFN of layer i mod 4 at position 4096 + i mod 256, the 28 layers
+    having the same shape; MoE stack: layer 0 at position 32768 + i mod 512), throughput scaled
+    by that layer's share of the token's algorithmic bytes. The sampled layers' weights are
+    decoded to fp64 before the warm-up (MoE experts as the oracle selects them, then kept), so a
+    run of K steps stays within minutes and a few GB of host memory."""
     if int(os.environ.get("RANK", "0")) != 0:
         return  # the oracle runs once, on rank 0; other ranks exit without work
     import synth
+    from synth import model as sm
     from oracle.model import OracleModel
     from persistent_megakernel_gb300 import roofline as R
-    s, layers, head, kv = build_workload(args.seed)
-    orc = OracleModel(s, layers, head, kv=kv, capacity=s.kv_prefill + CHAIN + 1, cache_weights=True)
+    if args.workload == "dense_2b":
+        s, layers, head, kv = build_workload(args.seed)
+        chain, ref_layers = CHAIN, 4
+        orc = OracleModel(s, layers, head, kv=kv, capacity=s.kv_prefill + chain + 1, cache_weights=True)
+    else:
+        s = workload_shape(args.workload)
+        chain, ref_layers = s.steps, 1
+        orc = OracleModel(s.with_(n_layers=1), [sm.layer_weights(s, args.seed, 0)], sm.head_weights(s, args.seed),
+                          experts=lambda l, e: sm.expert_weights(s, args.seed, 0, e),
+                          kv=[sm.kv_prefill(s, args.seed, 0)], capacity=s.kv_prefill + chain + 1, cache_weights=True)
     x = orc.embed(synth.start_token(args.seed, s.vocab))
     per_token = R.algorithmic_bytes(s, s.kv_prefill)
     layer_bytes = R.layer_weight_bytes(s) + R.kv_bytes(s, s.kv_prefill) / s.n_layers
 
-    ref_layers = 4
-
     def one(i):
-        l, pos = i % ref_layers, s.kv_prefill + (i % CHAIN)
+        l, pos = i % ref_layers, s.kv_prefill + (i % chain)
         y = orc.attention_block(l, x, pos)
         orc.ffn_block(l, y, {})
 
@@ -216,27 +270,26 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"dense_2b: {s.n_layers} layers, hidden 2560, GQA 20/4 x 128, FFN 6912, vocab 32768, "
-                               "KV prefill 4096, batch 1", "step": "one decoder layer of one token"},
+        "config": {"workload": WORKLOADS[args.workload].format(L=s.n_layers), "step": "one decoder layer of one token"},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                         "sample": "one decoder layer (attention + FFN, layers 0-3 in turn) per step, fp64 numpy, "
-                                   "weights decoded once before timing"},
+                         "sample": f"one decoder layer (attention + FFN, layers 0-{ref_layers - 1} in turn) per step, "
+                                   "fp64 numpy, weights decoded once before timing"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }))
 
 
-def timed_generate(dec, ctx_handle, tok0, pos0, K, launches_per_step):
-    """K greedy steps in chains of CHAIN on the device; returns (seconds by CUDA events, launches)."""
+def timed_generate(dec, ctx_handle, tok0, pos0, K, launches_per_step, chain=CHAIN):
+    """K greedy steps in chains of `chain` on the device; returns (seconds by CUDA events, launches)."""
     import torch
     from persistent_megakernel_gb300 import binding as B
-    out = torch.empty(CHAIN, dtype=torch.int32, device=dec.device)
+    out = torch.empty(chain, dtype=torch.int32, device=dec.device)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     e0.record(dec.stream)
     done, launches = 0, 0
     while done < K:
-        n = min(CHAIN, K - done)
+        n = min(chain, K - done)
         B.dec_generate(ctx_handle, tok0, pos0, n, out)
         launches += B.dec_last_launch_count(ctx_handle)
         done += n
@@ -255,6 +308,7 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-compare", action="store_true", help="skip the launch-per-op comparison")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="dense_2b", choices=sorted(WORKLOADS))
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling captures only: fewer decoder layers (the line is then not the workload's)")
     args = ap.parse_args()
@@ -273,19 +327,27 @@ def main():
 
     dev = f"cuda:{local}"
     torch.cuda.set_device(local)
-    s, layers, head, kv = build_workload(args.seed, args.layers)
-    cap = s.kv_prefill + CHAIN + 8
-    dec = Decoder(s, layers, head, kv=kv, capacity=cap, mode=args.mode, device=dev)
+    chain = CHAIN
+    layers = head = kv = None
+    if args.workload == "dense_2b":
+        s, layers, head, kv = build_workload(args.seed, args.layers)
+        cap = s.kv_prefill + chain + 8
+        dec = Decoder(s, layers, head, kv=kv, capacity=cap, mode=args.mode, device=dev)
+    else:
+        from tests.device_inputs import device_decoder
+        s = workload_shape(args.workload, args.layers)
+        chain = s.steps
+        dec = device_decoder(s, args.seed, s.kv_prefill + chain + 8, dev, mode=args.mode)
     tok0 = synth.start_token(args.seed, s.vocab)
     pos0 = s.kv_prefill
 
     # warm-up, then exactly K timed steps bracketed by barrier + synchronize
-    timed_generate(dec, dec.ctx, tok0, pos0, args.warmup, 1)
+    timed_generate(dec, dec.ctx, tok0, pos0, args.warmup, 1, chain)
     clocks = Clocks(local)
     clocks.start()
     barrier(ws)
     torch.cuda.synchronize()
-    secs, launches = timed_generate(dec, dec.ctx, tok0, pos0, args.steps, 1)
+    secs, launches = timed_generate(dec, dec.ctx, tok0, pos0, args.steps, 1, chain)
     torch.cuda.synchronize()
     barrier(ws)
     clk = clocks.stop()
@@ -293,15 +355,15 @@ def main():
     value = whole_job_rate(args.steps, secs, ws)
 
     # algorithmic bytes per step averaged over the positions the timed steps used
-    poss = [pos0 + (i % CHAIN) for i in range(args.steps)]
+    poss = [pos0 + (i % chain) for i in range(args.steps)]
     bytes_step = float(np.mean([R.algorithmic_bytes(s, p) for p in poss]))
     launch_s = secs / launches
     peak, peak_kind = peaks()
     achieved = bytes_step * (1 if args.mode == "persistent" else 1) / (secs / args.steps) / 1e9
-    traffic = ncu_traffic("megakernel_dense_2b.md", kernel_sources()) if args.mode == "persistent" else None
+    traffic = ncu_traffic(f"megakernel_{args.workload}.md", kernel_sources()) if args.mode == "persistent" else None
 
     # end to end through the C ABI with host buffers: token in, argmax out, every step
-    K2 = min(args.steps, CHAIN)
+    K2 = min(args.steps, chain)
     tok = tok0
     torch.cuda.synchronize()
     t0 = time.perf_counter()
@@ -314,11 +376,11 @@ def main():
     compare = None
     if not args.no_compare and args.mode == "persistent":
         compare = {}
-        Kc = min(args.steps, CHAIN)
+        Kc = min(args.steps, chain)
         for mode in ("per_op", "graph"):
             ctx, wsb = dec.context(mode)
-            timed_generate(dec, ctx, tok0, pos0, 4, 1)
-            t, L = timed_generate(dec, ctx, tok0, pos0, Kc, 1)
+            timed_generate(dec, ctx, tok0, pos0, 4, 1, chain)
+            t, L = timed_generate(dec, ctx, tok0, pos0, Kc, 1, chain)
             compare[mode] = {"tokens_s": Kc / t, "launches_per_step": L / Kc, "steps": Kc}
             B.dec_free(ctx)
             del wsb
@@ -326,16 +388,18 @@ def main():
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(s, layers, head, kv, args.seed)
+        cpu = cpu_baseline(s, layers, head, kv, args.seed) if layers is not None else cpu_baseline_layer(s, args.seed)
 
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * secs_max / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": f"dense_2b: {s.n_layers} layers, hidden 2560, GQA 20/4 x 128, SwiGLU 6912, vocab 32768, "
-                                   "KV prefill 4096, batch 1, greedy, chains of 256 steps (pos 4096-4351)",
-                       "weights": "bf16 ~N(0,0.02) seeded, accumulate fp32", "mode": args.mode,
+            "config": {"workload": WORKLOADS[args.workload].format(L=s.n_layers),
+                       "weights": ("bf16 ~N(0,0.02) seeded, accumulate fp32" if args.workload == "dense_2b" else
+                                   "bf16 attention / router / embedding, MXFP4 experts and FP8 head quantised from "
+                                   "seeded bf16 ~N(0,0.02), drawn and packed on the device; accumulate fp32"),
+                       "mode": args.mode,
                        "l2": "no flush: each step streams %.2f GB > 129 MB L2" % (bytes_step / 1e9),
                        "parallelism": f"replicas x{ws}"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",

@@ -235,6 +235,20 @@ dec_status dec_pack(dec_dtype dtype, const uint16_t* bf16_host, int rows, int co
 dec_status dec_pack_pair(dec_dtype dtype, const uint16_t* a_host, const uint16_t* b_host, int rows,
                          int cols, void* out_values, void* out_scales);
 
+/* ---------------------------------------------------------------- packer (device)
+   dec_pack / dec_pack_pair on device memory, for weights too large to stage through the host
+   (the MoE stack holds 67 GB of MXFP4 experts). Same rules and the same bytes as the host
+   packer: both run one set of encoders. bf16_dev (a_dev, b_dev): bf16 [rows][cols] on the
+   device; out_values / out_scales: device buffers of dec_packed_bytes. Inputs and out_values
+   16-byte aligned, FP8 out_scales 4-byte aligned (DEC_ERR_INVALID_ARG otherwise). The kernel is queued on `stream` (a cudaStream_t; NULL:
+   the legacy default stream) and the call returns without waiting; launch errors come back as
+   DEC_ERR_CUDA. The packer has no counterpart in the pages beyond the formats it writes. */
+dec_status dec_pack_device(dec_dtype dtype, const uint16_t* bf16_dev, int rows, int cols,
+                           void* out_values, void* out_scales, void* stream);
+dec_status dec_pack_pair_device(dec_dtype dtype, const uint16_t* a_dev, const uint16_t* b_dev,
+                                int rows, int cols, void* out_values, void* out_scales,
+                                void* stream);
+
 #ifdef __cplusplus
 }
 #endif

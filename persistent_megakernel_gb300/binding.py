@@ -36,7 +36,7 @@ DEC_MODE_PER_OP_GRAPH = 2
 # every symbol include/dec.h declares
 EXPORTS = ("dec_workspace_bytes", "dec_init", "dec_load_weights", "dec_set_kv_cache", "dec_step", "dec_generate",
            "dec_verify", "dec_debug_buffers", "dec_reset", "dec_sync", "dec_last_launch_count", "dec_last_error",
-           "dec_free", "dec_packed_bytes", "dec_pack", "dec_pack_pair", "dec_trace_buffer", "dec_lm_head_noalloc", "dec_debug_drop_op")
+           "dec_free", "dec_packed_bytes", "dec_pack", "dec_pack_pair", "dec_pack_device", "dec_pack_pair_device", "dec_trace_buffer", "dec_lm_head_noalloc", "dec_debug_drop_op")
 
 
 class DecConfig(ctypes.Structure):
@@ -88,6 +88,8 @@ def lib():
             "dec_packed_bytes": (I, [I, I, I, ctypes.POINTER(SZ), ctypes.POINTER(SZ)]),
             "dec_pack": (I, [I, P, I, I, P, P]),
             "dec_pack_pair": (I, [I, P, P, I, I, P, P]),
+            "dec_pack_device": (I, [I, P, I, I, P, P, P]),
+            "dec_pack_pair_device": (I, [I, P, P, I, I, P, P, P]),
             "dec_lm_head_noalloc": (I, [I, I, I, I, ctypes.c_float, P, P, P, P, P, P, P]),
         }
         for name, (res, args) in sig.items():
@@ -210,3 +212,14 @@ def dec_pack(dtype: int, w_bf16, rows: int, cols: int, out_values, out_scales=No
 
 def dec_pack_pair(dtype: int, a_bf16, b_bf16, rows: int, cols: int, out_values, out_scales=None) -> None:
     check(lib().dec_pack_pair(dtype, _p(a_bf16), _p(b_bf16), rows, cols, _p(out_values), _p(out_scales)))
+
+
+def dec_pack_device(dtype: int, w_bf16_dev, rows: int, cols: int, out_values_dev, out_scales_dev=None, stream=None) -> None:
+    """dec_pack on device buffers, queued on `stream` (a cudaStream_t handle or None)."""
+    check(lib().dec_pack_device(dtype, _p(w_bf16_dev), rows, cols, _p(out_values_dev), _p(out_scales_dev), _p(stream)))
+
+
+def dec_pack_pair_device(dtype: int, a_dev, b_dev, rows: int, cols: int, out_values_dev, out_scales_dev=None,
+                         stream=None) -> None:
+    check(lib().dec_pack_pair_device(dtype, _p(a_dev), _p(b_dev), rows, cols, _p(out_values_dev), _p(out_scales_dev),
+                                     _p(stream)))

@@ -22,6 +22,8 @@ using namespace decimpl;
 
 extern "C" cudaError_t dec_launch_megakernel(const KParams* kp, int cooperative, cudaStream_t stream);
 extern "C" int dec_megakernel_common_bytes(void);
+extern "C" cudaError_t dec_launch_pack(int dtype, const uint16_t* a, const uint16_t* b, int rows, int cols,
+                                       void* vals, void* scales, cudaStream_t stream);
 
 namespace {
 
@@ -1030,6 +1032,31 @@ dec_status dec_lm_head_noalloc(int hidden, int vocab, dec_dtype dtype, int m, fl
     return fail((dec_status)sw.code, "device wait timed out in the allocation-free LM head (cta %d, site %u)", sw.cta,
                 sw.where);
   return DEC_OK;
+}
+
+static dec_status pack_device(dec_dtype dtype, const uint16_t* a, const uint16_t* b, int rows, int cols, void* vals,
+                              void* scales, void* stream) {
+  size_t vb = 0, sb = 0;
+  const dec_status st = dec_packed_bytes(dtype, rows, cols, &vb, &sb);
+  if (st != DEC_OK) return fail(st, "cannot pack dtype %d as a [%d][%d] matrix", (int)dtype, rows, cols);
+  if (!a || !vals || (dtype != DEC_BF16 && !scales)) return fail(DEC_ERR_INVALID_ARG, "null device pointer");
+  const auto misaligned = [](const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) & (n - 1)) != 0; };
+  if (misaligned(a, 16) || (b && misaligned(b, 16)) || misaligned(vals, 16) ||
+      (dtype == DEC_FP8_E4M3_ROWSCALE && misaligned(scales, 4)))
+    return fail(DEC_ERR_INVALID_ARG, "device packer: inputs and values must be 16-byte aligned (FP8 scales 4-byte)");
+  CUDA_TRY(dec_launch_pack((int)dtype, a, b, rows, cols, vals, scales, static_cast<cudaStream_t>(stream)));
+  return DEC_OK;
+}
+
+dec_status dec_pack_device(dec_dtype dtype, const uint16_t* bf16_dev, int rows, int cols, void* out_values,
+                           void* out_scales, void* stream) {
+  return pack_device(dtype, bf16_dev, nullptr, rows, cols, out_values, out_scales, stream);
+}
+
+dec_status dec_pack_pair_device(dec_dtype dtype, const uint16_t* a_dev, const uint16_t* b_dev, int rows, int cols,
+                                void* out_values, void* out_scales, void* stream) {
+  if (!b_dev) return fail(DEC_ERR_INVALID_ARG, "null device pointer");
+  return pack_device(dtype, a_dev, b_dev, rows, cols, out_values, out_scales, stream);
 }
 
 void dec_free(dec_ctx* c) {

@@ -69,16 +69,37 @@ def pack_host(dtype: int, w: np.ndarray, pair_with: np.ndarray | None = None):
     return vals, (scales[:sb] if sb else None)
 
 
+def pack_device(dtype: int, w: torch.Tensor, pair_with: torch.Tensor | None = None):
+    """Pack one logical bf16 matrix held on the device (2-byte elements, [rows, cols]), or two
+    interleaved row by row, with the library's device packer on the current stream."""
+    rows, cols = w.shape
+    out_rows = rows * (2 if pair_with is not None else 1)
+    vb, sb = B.dec_packed_bytes(dtype, out_rows, cols)
+    vals = torch.empty(vb, dtype=torch.uint8, device=w.device)
+    scales = torch.empty(max(sb, 1), dtype=torch.uint8, device=w.device) if sb else None
+    stream = torch.cuda.current_stream(w.device).cuda_stream
+    if pair_with is None:
+        B.dec_pack_device(dtype, w, rows, cols, vals, scales, stream)
+    else:
+        B.dec_pack_pair_device(dtype, w, pair_with, rows, cols, vals, scales, stream)
+    return vals, scales
+
+
 class Decoder:
     """One model instance on one GPU: workspace, packed weights, KV cache, context.
 
     shape      : a ModelShape (dims, eps, RoPE base, head dtype, embedding)
     layers     : per-layer dicts of logical bf16 weights (attn_norm, w_qkv, w_o, ffn_norm,
-                 w_gate, w_up, w_down, w_router)
+                 w_gate, w_up, w_down, w_router): numpy uint16 arrays (packed on the host) or
+                 2-byte device tensors (packed on the device)
     head       : dict with embed / final_norm / w_lm
     experts    : callable (layer, expert) -> (gate, up, down) bf16 for MoE layers; experts
                  shape.n_experts .. + n_shared - 1 are the shared ones
-    kv         : list of (K, V) bf16 prefills [n_kv, n, d] per layer, or None
+    kv         : list of (K, V) bf16 prefills [n_kv, n, d] per layer, or None (the caller may
+                 fill ``k_cache`` / ``v_cache`` itself before the first step)
+    packed_experts : instead of ``experts``, callable layer -> (gate/up values, gate/up scales,
+                 down values, down scales), the MXFP4 planes of all the layer's experts already
+                 packed (host arrays or device tensors)
     """
 
     def __init__(self, shape, layers, head, experts=None, kv=None, capacity=None, max_verify=1, mode="persistent",
@@ -118,7 +139,8 @@ class Decoder:
             if s.ffn or s.moe:
                 reg(B.DEC_T_FFN_NORM, l, B.DEC_BF16, H, 1, w["ffn_norm"])
             if s.ffn:
-                vals, _ = pack_host(B.DEC_BF16, w["w_gate"], w["w_up"])
+                pack = pack_device if isinstance(w["w_gate"], torch.Tensor) else pack_host
+                vals, _ = pack(B.DEC_BF16, w["w_gate"], w["w_up"])
                 reg(B.DEC_T_WGATEUP, l, B.DEC_BF16, 2 * s.ffn, H, vals)
                 reg(B.DEC_T_WDOWN, l, B.DEC_BF16, H, s.ffn, w["w_down"])
             if s.moe:
@@ -135,7 +157,8 @@ class Decoder:
             if s.final_norm:
                 reg(B.DEC_T_FINAL_NORM, 0, B.DEC_BF16, H, 1, head["final_norm"])
             if s.lm_head_dtype == "fp8":
-                vals, scales = pack_host(B.DEC_FP8_E4M3_ROWSCALE, head["w_lm"])
+                pack = pack_device if isinstance(head["w_lm"], torch.Tensor) else pack_host
+                vals, scales = pack(B.DEC_FP8_E4M3_ROWSCALE, head["w_lm"])
                 reg(B.DEC_T_LM_HEAD, 0, B.DEC_FP8_E4M3_ROWSCALE, s.vocab, H, vals, scales)
             else:
                 reg(B.DEC_T_LM_HEAD, 0, B.DEC_BF16, s.vocab, H, head["w_lm"])

@@ -1,14 +1,17 @@
 """Seeded synthetic inputs shared by the CUDA path's tests, the bench and the oracle.
 
 Holds input generation only (counter-based draws, tensor naming, model
-shapes); none of the decode step's arithmetic lives here. The C source
-``gen.c`` states the generator's definition; this wrapper compiles it on first
-use and returns numpy arrays of bfloat16 bits (``uint16``) or fp64 values.
+shapes); none of the decode step's arithmetic lives here. The header
+``gen_core.h`` states the generator's definition; ``gen.c`` runs it on the host
+(this wrapper compiles it on first use and returns numpy arrays of bfloat16 bits
+(``uint16``) or fp64 values) and ``gen_dev.cu`` on the GPU, writing device
+memory directly for weights too large to draw on the host.
 """
 from __future__ import annotations
 
 import ctypes
 import os
+import shutil
 import subprocess
 import threading
 
@@ -26,14 +29,19 @@ from .configs import (  # noqa: F401
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gen.c")
+_CORE = os.path.join(_HERE, "gen_core.h")
 _LIB = os.path.join(_HERE, "libsynth.so")
+_DEV_SRC = os.path.join(_HERE, "gen_dev.cu")
+_DEV_LIB = os.path.join(_HERE, "libsynth_dev.so")
 _lock = threading.Lock()
 _lib = None
+_dev_lib = None
 
 
 def build(force: bool = False) -> str:
     """Compile ``gen.c`` into ``libsynth.so`` next to it (gcc, OpenMP)."""
-    stale = force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC)
+    stale = force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < max(
+        os.path.getmtime(_SRC), os.path.getmtime(_CORE))
     if stale:
         tmp = _LIB + f".tmp{os.getpid()}"
         subprocess.check_call(
@@ -41,6 +49,47 @@ def build(force: bool = False) -> str:
         )
         os.replace(tmp, _LIB)
     return _LIB
+
+
+def build_device(force: bool = False) -> str:
+    """Compile ``gen_dev.cu`` into ``libsynth_dev.so`` (nvcc, sm_103a, no fused multiply-add)."""
+    stale = force or not os.path.exists(_DEV_LIB) or os.path.getmtime(_DEV_LIB) < max(
+        os.path.getmtime(_DEV_SRC), os.path.getmtime(_CORE))
+    if stale:
+        nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+        tmp = _DEV_LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(
+            [nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-fmad=false", "-std=c++17",
+             "-Xcompiler", "-fPIC", "-shared", _DEV_SRC, "-o", tmp]
+        )
+        os.replace(tmp, _DEV_LIB)
+    return _DEV_LIB
+
+
+def _get_dev():
+    global _dev_lib
+    with _lock:
+        if _dev_lib is None:
+            if not os.path.exists(_DEV_LIB):
+                raise ImportError(f"{_DEV_LIB} is missing: build it with synth.build_device()")
+            lib = ctypes.CDLL(_DEV_LIB)
+            u64, dbl, ptr = ctypes.c_uint64, ctypes.c_double, ctypes.c_void_p
+            lib.synth_normal_bf16_dev.restype = ctypes.c_int
+            lib.synth_normal_bf16_dev.argtypes = [u64, u64, u64, u64, dbl, dbl, ptr, ptr]
+            _dev_lib = lib
+    return _dev_lib
+
+
+def normal_bf16_dev(out, seed: int, tid: int, mean: float = 0.0, std: float = 1.0, start: int = 0,
+                    stream=None) -> None:
+    """Fill the contiguous 2-byte device tensor ``out`` with the bf16 bits of draws
+    ``start..start+out.numel()-1`` of stream ``tid`` (the values :func:`normal_bf16` returns),
+    queued on ``stream`` (a cudaStream_t handle; None: the legacy default stream)."""
+    if out.element_size() != 2 or not out.is_contiguous():
+        raise ValueError("normal_bf16_dev writes a contiguous tensor of 2-byte elements")
+    rc = _get_dev().synth_normal_bf16_dev(seed, tid, start, out.numel(), mean, std, out.data_ptr(), stream)
+    if rc != 0:
+        raise RuntimeError(f"synth_normal_bf16_dev: CUDA error {rc}")
 
 
 def _get():

@@ -4,111 +4,58 @@
  * This file holds input generation only. It computes nothing of the decode
  * step itself; both the CUDA path and the CPU oracle receive what it writes.
  *
- * Definition (every function below follows it exactly):
- *   SplitMix64 (Steele, Lea, Flood, "Fast splittable pseudorandom number
- *   generators", OOPSLA 2014): gamma = 0x9E3779B97F4A7C15 and the 64-bit
- *   finaliser mix64(z) = z3 where z1 = (z ^ z>>30) * 0xBF58476D1CE4E5B9,
- *   z2 = (z1 ^ z1>>27) * 0x94D049BB133111EB, z3 = z2 ^ z2>>31.
- *   stream key   K(seed, tid) = mix64(mix64(seed + gamma) ^ tid)
- *   i-th draw    B(K, i)      = mix64(K + (i + 1) * gamma)       (mod 2^64)
- *   Box-Muller (Box & Muller 1958) on draws 2p and 2p+1:
- *     u1 = ((B(K,2p)   >> 11) + 1) * 2^-53   in (0, 1]
- *     u2 =  (B(K,2p+1) >> 11)      * 2^-53   in [0, 1)
- *     r  = sqrt(-2 ln u1);  z[2p] = r cos(2 pi u2);  z[2p+1] = r sin(2 pi u2)
- *   value = mean + std * z  (fp64), then rounded to bfloat16 with
- *   round-to-nearest-even directly from the fp64 bits (no fp32 step).
+ * The generator's definition (SplitMix64 streams, Box-Muller normals, fp64 -> bf16
+ * rounding) is stated in gen_core.h, which the device library gen_dev.cu shares.
  *
  * Built as a plain shared library (gcc -O2 -fopenmp -shared -fPIC); the
  * Python wrapper in this folder calls it through ctypes.
  */
-#include <math.h>
-#include <stdint.h>
-#include <string.h>
+#include "gen_core.h"
 
-#define SM_GAMMA 0x9E3779B97F4A7C15ULL
+uint64_t synth_stream_key(uint64_t seed, uint64_t tid) { return sg_stream_key(seed, tid); }
 
-static inline uint64_t mix64(uint64_t z) {
-  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ULL;
-  z = (z ^ (z >> 27)) * 0x94D049BB133111EBULL;
-  return z ^ (z >> 31);
-}
+uint64_t synth_draw(uint64_t key, uint64_t i) { return sg_draw(key, i); }
 
-uint64_t synth_stream_key(uint64_t seed, uint64_t tid) {
-  return mix64(mix64(seed + SM_GAMMA) ^ tid);
-}
-
-uint64_t synth_draw(uint64_t key, uint64_t i) { return mix64(key + (i + 1) * SM_GAMMA); }
-
-/* Round an IEEE double to bfloat16 bits, nearest-even, NaN kept quiet. */
-uint16_t synth_f64_to_bf16(double v) {
-  uint64_t b;
-  memcpy(&b, &v, 8);
-  uint16_t sign = (uint16_t)((b >> 48) & 0x8000u);
-  uint64_t mag = b & 0x7FFFFFFFFFFFFFFFULL;
-  if (mag > 0x7FF0000000000000ULL) return (uint16_t)(sign | 0x7FC0u); /* NaN */
-  if (mag == 0x7FF0000000000000ULL) return (uint16_t)(sign | 0x7F80u); /* inf */
-  int e = (int)(mag >> 52);           /* biased fp64 exponent */
-  uint64_t m = mag & ((1ULL << 52) - 1);
-  int E = e - 1023;                   /* unbiased */
-  /* bf16: 8 exponent bits (bias 127), 7 mantissa bits, subnormals below 2^-126 */
-  if (e == 0) return sign;            /* fp64 subnormals are far below bf16's range */
-  uint64_t sig = m | (1ULL << 52);    /* 53-bit significand, value = sig * 2^(E-52) */
-  int shift;                          /* bits to drop from sig */
-  uint32_t out_exp;
-  if (E >= -126) {
-    shift = 52 - 7;
-    out_exp = (uint32_t)(E + 127);
-  } else {
-    /* subnormal bf16: value = q * 2^-133, q = sig * 2^(E-52+133) */
-    shift = 52 - 7 + (-126 - E);
-    out_exp = 0;
-    if (shift > 60) return sign;
-  }
-  uint64_t q = sig >> shift;
-  uint64_t rem = sig & ((1ULL << shift) - 1);
-  uint64_t half = 1ULL << (shift - 1);
-  if (rem > half || (rem == half && (q & 1))) q += 1;
-  uint32_t bits;
-  if (out_exp == 0) {
-    bits = (uint32_t)q; /* q <= 2^7; q == 2^7 carries into the smallest normal */
-  } else {
-    /* q in [2^7, 2^8]; a carry to 2^8 bumps the exponent */
-    if (q == (1ULL << 8)) { q >>= 1; out_exp += 1; }
-    if (out_exp >= 255) return (uint16_t)(sign | 0x7F80u);
-    bits = (out_exp << 7) | (uint32_t)(q & 0x7F);
-  }
-  return (uint16_t)(sign | bits);
-}
-
-static inline double unit_open0(uint64_t bits) { return (double)((bits >> 11) + 1) * 0x1.0p-53; }
-static inline double unit_closed0(uint64_t bits) { return (double)(bits >> 11) * 0x1.0p-53; }
+uint16_t synth_f64_to_bf16(double v) { return sg_f64_to_bf16(v); }
 
 /* Standard normal draw number idx of stream key. */
 double synth_normal_at(uint64_t key, uint64_t idx) {
-  uint64_t p = idx >> 1;
-  double u1 = unit_open0(synth_draw(key, 2 * p));
-  double u2 = unit_closed0(synth_draw(key, 2 * p + 1));
-  double r = sqrt(-2.0 * log(u1));
-  double a = 6.283185307179586476925286766559 * u2;
-  return (idx & 1) ? r * sin(a) : r * cos(a);
+  double z0, z1;
+  sg_normal_pair(key, idx >> 1, &z0, &z1);
+  return (idx & 1) ? z1 : z0;
 }
 
-/* out[i] = bf16(mean + std * z[start + i]) for i in [0, n). */
+/* out[i] = bf16(mean + std * z[start + i]) for i in [0, n). Each Box-Muller pair is evaluated
+   once and gives both of its draws. */
 void synth_normal_bf16(uint64_t seed, uint64_t tid, uint64_t start, uint64_t n, double mean,
                        double std, uint16_t* out) {
-  uint64_t key = synth_stream_key(seed, tid);
+  if (n == 0) return;
+  const uint64_t key = synth_stream_key(seed, tid);
+  const uint64_t p0 = start >> 1, p1 = (start + n - 1) >> 1;
 #pragma omp parallel for schedule(static)
-  for (long long i = 0; i < (long long)n; ++i)
-    out[i] = synth_f64_to_bf16(mean + std * synth_normal_at(key, start + (uint64_t)i));
+  for (long long q = 0; q <= (long long)(p1 - p0); ++q) {
+    const uint64_t p = p0 + (uint64_t)q;
+    double z0, z1;
+    sg_normal_pair(key, p, &z0, &z1);
+    if (2 * p >= start) out[2 * p - start] = sg_f64_to_bf16(mean + std * z0);
+    if (2 * p + 1 < start + n) out[2 * p + 1 - start] = sg_f64_to_bf16(mean + std * z1);
+  }
 }
 
 /* out[i] = mean + std * z[start + i] in fp64 (for inputs the method keeps in full precision). */
 void synth_normal_f64(uint64_t seed, uint64_t tid, uint64_t start, uint64_t n, double mean,
                       double std, double* out) {
-  uint64_t key = synth_stream_key(seed, tid);
+  if (n == 0) return;
+  const uint64_t key = synth_stream_key(seed, tid);
+  const uint64_t p0 = start >> 1, p1 = (start + n - 1) >> 1;
 #pragma omp parallel for schedule(static)
-  for (long long i = 0; i < (long long)n; ++i)
-    out[i] = mean + std * synth_normal_at(key, start + (uint64_t)i);
+  for (long long q = 0; q <= (long long)(p1 - p0); ++q) {
+    const uint64_t p = p0 + (uint64_t)q;
+    double z0, z1;
+    sg_normal_pair(key, p, &z0, &z1);
+    if (2 * p >= start) out[2 * p - start] = mean + std * z0;
+    if (2 * p + 1 < start + n) out[2 * p + 1 - start] = mean + std * z1;
+  }
 }
 
 /* out[i] = B(K(seed, tid), start + i): raw 64-bit draws. */

@@ -110,6 +110,73 @@ def test_mxfp4_packer_equals_oracle_quantiser(B):
     assert np.array_equal(codes.reshape(-1), vals)
 
 
+def _finite_bf16_upto(limit_bits: int) -> np.ndarray:
+    """Every finite bf16 bit pattern (both signs) whose magnitude is at most limit_bits."""
+    allb = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    mag = allb & 0x7FFF
+    return allb[(mag < 0x7F80) & (mag <= limit_bits)]
+
+
+def _bits(x: float) -> int:
+    return int(np.array([x], np.float32).view(np.uint32)[0] >> 16)
+
+
+@pytest.mark.parametrize("amax", [1.0, 448.0, 3e-5, 1e30, 0.02, 7.5, 3.3e38, 2.0 ** -130])
+def test_fp8_packer_every_bf16_value(B, amax):
+    # rows [amax, v ...] with every finite |v| <= amax: each e4m3 code and rounding tie is reached
+    vals = _finite_bf16_upto(_bits(amax))
+    cols = 512
+    rows = -(-len(vals) // (cols - 1))
+    w = np.zeros((rows, cols), np.uint16)
+    w[:, 0] = _bits(amax)
+    flat = np.zeros(rows * (cols - 1), np.uint16)
+    flat[:len(vals)] = vals
+    w[:, 1:] = flat.reshape(rows, cols - 1)
+    out = np.empty(rows * cols, np.uint8)
+    sc = np.empty(rows, np.float32)
+    B.dec_pack(B.DEC_FP8_E4M3_ROWSCALE, w, rows, cols, out, sc)
+    codes, s = F.quantize_fp8_rows(w)
+    assert np.array_equal(s, sc)
+    assert np.array_equal(codes.reshape(-1), out)
+
+
+@pytest.mark.parametrize("bmax", [1.0, 6.0, 5.0, 0.75, 2.0 ** -133, 2.0 ** -126, 1e30, 3.3e38])
+def test_mxfp4_packer_every_bf16_value(B, bmax):
+    # blocks [bmax, 31 values with |v| <= bmax], the maximum at a seeded position of each block
+    vals = _finite_bf16_upto(_bits(bmax))
+    nb = -(-len(vals) // 31)
+    nb += (-nb) % 32
+    blocks = np.zeros((nb, 32), np.uint16)
+    flat = np.zeros(nb * 31, np.uint16)
+    flat[:len(vals)] = vals
+    blocks[:, 1:] = flat.reshape(nb, 31)
+    blocks[:, 0] = _bits(bmax)
+    perm = np.argsort(synth.bits(7, 506, nb * 32).reshape(nb, 32), axis=1)
+    blocks = np.take_along_axis(blocks, perm, axis=1)
+    w = np.ascontiguousarray(blocks.reshape(-1, 1024))
+    rows = w.shape[0]
+    out = np.empty(rows * 512, np.uint8)
+    sc = np.empty(rows * 32, np.uint8)
+    B.dec_pack(B.DEC_MXFP4, w, rows, 1024, out, sc)
+    codes, e = F.quantize_mxfp4(w)
+    assert np.array_equal(e.reshape(-1), sc)
+    assert np.array_equal(codes.reshape(-1), out)
+
+
+def test_device_packer_rejects_bad_arguments(B):
+    # checked on the host before any launch, so no GPU is needed
+    L = B.lib()
+    ok = 0x10000
+    assert L.dec_pack_device(B.DEC_MXFP4, None, 4, 64, ok, ok, None) == B.DEC_ERR_INVALID_ARG
+    assert L.dec_pack_device(B.DEC_MXFP4, ok, 4, 64, ok, None, None) == B.DEC_ERR_INVALID_ARG
+    assert L.dec_pack_device(B.DEC_MXFP4, ok + 8, 4, 64, ok, ok, None) == B.DEC_ERR_INVALID_ARG
+    assert L.dec_pack_device(B.DEC_MXFP4, ok, 4, 48, ok, ok, None) == B.DEC_ERR_SHAPE
+    assert L.dec_pack_device(B.DEC_FP8_E4M3_ROWSCALE, ok, 4, 64, ok, ok + 2, None) == B.DEC_ERR_INVALID_ARG
+    assert L.dec_pack_device(7, ok, 4, 64, ok, ok, None) == B.DEC_ERR_DTYPE
+    assert L.dec_pack_pair_device(B.DEC_BF16, ok, None, 4, 64, ok, None, None) == B.DEC_ERR_INVALID_ARG
+    assert "aligned" in B.dec_last_error() or "null" in B.dec_last_error()
+
+
 def test_pair_packer_interleaves_rows(B):
     a = synth.normal_bf16(5, 504, (6, 64), 0.0, 0.02)
     b = synth.normal_bf16(5, 505, (6, 64), 0.0, 0.02)
