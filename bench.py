@@ -94,16 +94,17 @@ class Clocks:
     def __init__(self, gpu_index: int):
         self.idx = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        self.path = os.path.join(ROOT, f".bench_clocks_{os.getpid()}.csv")
 
     def start(self):
+        self.f = open(self.path, "w")
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
-            self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}", "--format=csv",
                                           "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+            self.f.close()
+            os.remove(self.path)
 
     def stop(self):
         if self.proc is None:
@@ -115,7 +116,12 @@ class Clocks:
             self.proc.kill()
         self.f.close()
         rows = []
-        for ln in open(self.path).read().splitlines()[1:]:
+        text = open(self.path).read()
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        for ln in text.splitlines()[1:]:
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 9:
                 continue
