@@ -21,7 +21,10 @@ cache holds bfloat16, every product and sum taken in fp64:
 * the LM head may be the bf16 matrix or its dynamic FP8 quantisation
   (same article, section "optimisation 2: online FP8 LM head");
 * a verify window of k tokens is checked in one pass and the correct prefix
-  accepted (same article, section "optimisation 3: MTP speculative decoding").
+  accepted (same article, section "optimisation 3: MTP speculative decoding");
+* optionally the KV cache holds FP8 e4m3 codes with a scale per layer, K/V and
+  kv head, 1.0 unless given (Kimi-K3 on 8xB300: fp8_e4m3 caches whose missing
+  scaling factors fall back to 1.0).
 
 Modules: ``formats`` (number formats and the FP8 / MXFP4 quantisers),
 ``ops`` (one function per operation), ``model`` (the whole step and verify).

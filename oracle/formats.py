@@ -177,3 +177,24 @@ def dequant_mxfp4(codes, scales) -> np.ndarray:
     q[:, 1::2] = codes >> 4
     vals = e2m1_to_f64(q).reshape(R, -1, MX_BLOCK)
     return (vals * e8m0_to_f64(scales)[:, :, None]).reshape(R, half * 2)
+
+
+# ------------------------------------------------------------------ FP8 KV cache
+
+
+def quantize_kv_fp8(x, scale) -> np.ndarray:
+    """e4m3fn codes of KV-cache entries ``x`` under ``scale`` s (Kimi-K3 on 8xB300, section on
+    the log warnings: both engines keep the KV cache as fp8_e4m3, and without a calibrated
+    scaling factor they fall back to a scale of 1.0). The stored value is s * e4m3(q) with
+    q = e4m3_satfinite_RNE(x / s); x is taken in fp32 and the division is IEEE fp32 (the
+    precision the kernel computes a new key or value in). ``scale`` (fp32, > 0) broadcasts
+    against x, e.g. one scale per kv head."""
+    x32 = np.asarray(x, np.float64).astype(np.float32)
+    s32 = np.asarray(scale, np.float32)
+    y = (x32 / s32).astype(np.float32)
+    return round_e4m3_satfinite(y.astype(np.float64))
+
+
+def dequant_kv_fp8(codes, scale) -> np.ndarray:
+    """Value of FP8 KV-cache codes: s * e4m3(q), ``scale`` broadcasting against the codes."""
+    return e4m3_to_f64(codes) * np.asarray(scale, np.float32).astype(np.float64)

@@ -45,7 +45,8 @@ class OracleModel:
     capacity   : positions the oracle's own cache can hold
     """
 
-    def __init__(self, shape, layers, head, experts=None, kv=None, capacity=None, cache_weights=False):
+    def __init__(self, shape, layers, head, experts=None, kv=None, capacity=None, cache_weights=False,
+                 kv_scales=None):
         self.s = shape
         self.layers = layers
         self.head = head
@@ -55,17 +56,32 @@ class OracleModel:
         self._experts = {}
         self._lm = None
         cap = capacity if capacity is not None else shape.kv_prefill + 8
+        # FP8 cache (shape.kv_dtype == "fp8"): e4m3 codes, fp32 scales [layer][K, V][kv head];
+        # the engines' fallback scale 1.0 when none is given
+        self.kv_fp8 = getattr(shape, "kv_dtype", "bf16") == "fp8"
+        self.kv_scales = (np.ones((max(shape.n_layers, 1), 2, max(shape.n_kv, 1)), np.float32) if kv_scales is None
+                          else np.asarray(kv_scales, np.float32))
         self.K, self.V = [], []
         if shape.attn:
             for l in range(shape.n_layers):
-                K = np.zeros((shape.n_kv, cap, shape.head_dim), np.uint16)
+                K = np.zeros((shape.n_kv, cap, shape.head_dim), np.uint8 if self.kv_fp8 else np.uint16)
                 V = np.zeros_like(K)
                 if kv is not None:
                     n = kv[l][0].shape[1]
-                    K[:, :n] = kv[l][0]
-                    V[:, :n] = kv[l][1]
+                    if self.kv_fp8:
+                        # the prefilled bf16 history is stored quantised, like every new row
+                        K[:, :n] = F.quantize_kv_fp8(bf16_to_f64_fast(kv[l][0]), self._kv_scale(l, 0, 3))
+                        V[:, :n] = F.quantize_kv_fp8(bf16_to_f64_fast(kv[l][1]), self._kv_scale(l, 1, 3))
+                    else:
+                        K[:, :n] = kv[l][0]
+                        V[:, :n] = kv[l][1]
                 self.K.append(K)
                 self.V.append(V)
+
+    def _kv_scale(self, l, kv, ndim):
+        """Scales of layer l's keys (kv = 0) or values (1), one per kv head, shaped to broadcast
+        against an [n_kv, ...] array of ndim dimensions."""
+        return self.kv_scales[l, kv].reshape((-1,) + (1,) * (ndim - 1))
 
     # ---------------------------------------------------------------- weights
     def w(self, l, name):
@@ -111,11 +127,17 @@ class OracleModel:
         v = qkv[(s.n_q + s.n_kv) * d:].reshape(s.n_kv, d)
         q = ops.rope(q, pos, s.rope_base)
         k = ops.rope(k, pos, s.rope_base)
-        # the cache holds bf16: the new row is stored rounded, then read back (R4)
-        self.K[l][:, pos] = F.f64_to_bf16(k)
-        self.V[l][:, pos] = F.f64_to_bf16(v)
-        Kc = bf16_to_f64_fast(self.K[l][:, : pos + 1])
-        Vc = bf16_to_f64_fast(self.V[l][:, : pos + 1])
+        # the cache holds bf16 (or FP8 codes): the new row is stored rounded, then read back (R4)
+        if self.kv_fp8:
+            self.K[l][:, pos] = F.quantize_kv_fp8(k, self._kv_scale(l, 0, 2))
+            self.V[l][:, pos] = F.quantize_kv_fp8(v, self._kv_scale(l, 1, 2))
+            Kc = F.dequant_kv_fp8(self.K[l][:, : pos + 1], self._kv_scale(l, 0, 3))
+            Vc = F.dequant_kv_fp8(self.V[l][:, : pos + 1], self._kv_scale(l, 1, 3))
+        else:
+            self.K[l][:, pos] = F.f64_to_bf16(k)
+            self.V[l][:, pos] = F.f64_to_bf16(v)
+            Kc = bf16_to_f64_fast(self.K[l][:, : pos + 1])
+            Vc = bf16_to_f64_fast(self.V[l][:, : pos + 1])
         o = ops.attention(q, Kc, Vc)
         return x + ops.gemv(self.w(l, "w_o"), o.reshape(-1))
 
