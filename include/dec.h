@@ -156,7 +156,12 @@ dec_status dec_verify(dec_ctx* ctx, const int32_t* tokens_host, const void* hidd
    residual stream [2 n_layers + 1][max_verify][H] (entry 2l+1 after the attention block of
    layer l, entry 2l+2 after its FFN; entry 0 is unused, the input comes from the embedding
    or hidden_dev); qkv: the projections [n_layers][max_verify][qkv rows]; routing: one
-   routing block per MoE layer (n_slots, expert ids, slot weights, per-token top-k).
+   routing block per MoE layer, 920 bytes each, laid out as
+     int32 n_slots;          n_shared + the distinct routed experts of the call (<= 33)
+     int32 expert[33];       expert id per slot, shared experts first (id >= n_experts)
+     float w[4][33];         weight of each slot for token m (1 for shared, pi or 0)
+     int32 topk[4][8];       token m's routed experts, best first
+     float topk_w[4][8];     their weights pi
    For inspection and tests; valid until the next call on the stream. */
 dec_status dec_debug_buffers(dec_ctx* ctx, const uint64_t** hidden, const uint64_t** qkv,
                              const int32_t** routing);

@@ -246,19 +246,28 @@ class Decoder:
         words = self.ws[off:off + 8 * n].view(torch.float32).view(n, 2)
         return words[:, 0].contiguous().view(2 * s.n_layers + 1, self.max_verify, s.hidden)
 
+    # routing block of dec_debug_buffers (include/dec.h): int32 n_slots, int32 expert[33],
+    # float w[4][33], int32 topk[4][8], float topk_w[4][8]
+    ROUTE_SLOTS, ROUTE_TOKENS, ROUTE_K = 33, 4, 8
+    ROUTE_WORDS = 1 + ROUTE_SLOTS + ROUTE_TOKENS * ROUTE_SLOTS + 2 * ROUTE_TOKENS * ROUTE_K
+
     def routing(self, layer: int) -> dict:
         """Routing block of a MoE layer after the last call (slots, per-token top-k)."""
         _, _, r = B.dec_debug_buffers(self.ctx)
         off = r - self.ws.data_ptr()
-        sz = 4 * (1 + 33 + 4 * 33 + 4 * 8 + 4 * 8)
+        S, T, K = self.ROUTE_SLOTS, self.ROUTE_TOKENS, self.ROUTE_K
+        sz = 4 * self.ROUTE_WORDS
         raw = self.ws[off + layer * sz: off + (layer + 1) * sz].cpu().numpy()
         i32 = raw.view(np.int32)
         f32 = raw.view(np.float32)
         n = int(i32[0])
+        w0 = 1 + S                      # float w[T][S]
+        t0 = w0 + T * S                 # int32 topk[T][K]
+        tw0 = t0 + T * K                # float topk_w[T][K]
         return {"n_slots": n, "expert": i32[1:1 + n].tolist(),
-                "w": f32[34:34 + 4 * 33].reshape(4, 33)[:, :n],
-                "topk": i32[34 + 132: 34 + 132 + 32].reshape(4, 8),
-                "topk_w": f32[34 + 132 + 32: 34 + 132 + 64].reshape(4, 8)}
+                "w": f32[w0:t0].reshape(T, S)[:, :n],
+                "topk": i32[t0:tw0].reshape(T, K),
+                "topk_w": f32[tw0:tw0 + T * K].reshape(T, K)}
 
     def close(self):
         if self.ctx:

@@ -45,6 +45,28 @@ def test_struct_layouts_match_header(B):
     assert ctypes.sizeof(B.DecTensor) == 40 and B.DecTensor.values.offset == 24
 
 
+def test_routing_block_layout_matches_reader(tmp_path):
+    # the Python reader's offsets (model.Decoder.routing) against the struct the kernel writes,
+    # measured by a host compile of the internal header
+    import subprocess
+    from persistent_megakernel_gb300.model import Decoder
+    src = tmp_path / "rb.cpp"
+    src.write_text(
+        '#include <cstddef>\n#include <cstdio>\n#include "dec_internal.h"\nusing decimpl::RouteBlock;\n'
+        'int main() { std::printf("%zu %zu %zu %zu %zu\\n", sizeof(RouteBlock), offsetof(RouteBlock, expert), '
+        'offsetof(RouteBlock, w), offsetof(RouteBlock, topk), offsetof(RouteBlock, topk_w)); }\n')
+    exe = tmp_path / "rb"
+    csrc = os.path.join(ROOT, "persistent_megakernel_gb300", "csrc")
+    from persistent_megakernel_gb300 import build
+    cuda_inc = os.path.join(build._cuda_home(build._nvcc()), "include")
+    subprocess.check_call(["g++", "-std=c++17", "-I", csrc, "-I", os.path.join(ROOT, "include"), "-I", cuda_inc,
+                           str(src), "-o", str(exe)])
+    size, expert, w, topk, topk_w = map(int, subprocess.check_output([str(exe)]).split())
+    S, T, K = Decoder.ROUTE_SLOTS, Decoder.ROUTE_TOKENS, Decoder.ROUTE_K
+    assert size == 4 * Decoder.ROUTE_WORDS == 920
+    assert (expert, w, topk, topk_w) == (4, 4 * (1 + S), 4 * (1 + S + T * S), 4 * (1 + S + T * S + T * K))
+
+
 def _cfg(B, **kw):
     c = B.DecConfig()
     base = dict(n_layers=1, hidden=256, n_q=4, n_kv=2, head_dim=128, ffn=512, vocab=100, kv_capacity=64, max_verify=1,
