@@ -304,6 +304,73 @@ def timed_generate(dec, ctx_handle, tok0, pos0, K, launches_per_step, chain=CHAI
     return e0.elapsed_time(e1) * 1e-3, launches
 
 
+def run_verify(args, rank, ws, local):
+    """Verify windows of k tokens (the MTP verify step of the Ling-3.0-flash DGX Spark article,
+    "optimisation 3"): each call feeds the model's last prediction plus k-1 seeded draft tokens at
+    the next k positions, one window after another (positions advance by k, as if every draft
+    were accepted), and reads back the k argmaxes and the accepted count, so the host waits for
+    every window. value = window tokens per second; roofline = the window's algorithmic bytes
+    (weights once, the union of the window's experts, the KV rows read) over its time."""
+    import torch
+    import synth
+    from persistent_megakernel_gb300 import build as pbuild
+    pbuild.build()
+    from persistent_megakernel_gb300 import binding as B
+    from persistent_megakernel_gb300 import roofline as R
+    from persistent_megakernel_gb300.model import Decoder
+    k = args.verify
+    dev = f"cuda:{local}"
+    torch.cuda.set_device(local)
+    n_win = args.warmup + args.steps
+    if args.workload == "dense_2b":
+        s, layers, head, kv = build_workload(args.seed, args.layers)
+        cap = s.kv_prefill + k * n_win + 8
+        dec = Decoder(s, layers, head, kv=kv, capacity=cap, mode=args.mode, device=dev, max_verify=k)
+    else:
+        from tests.device_inputs import device_decoder
+        s = workload_shape(args.workload, args.layers)
+        cap = s.kv_prefill + k * n_win + 8
+        dec = device_decoder(s, args.seed, cap, dev, mode=args.mode, max_verify=k)
+    drafts = synth.bits(args.seed, synth.tensor_id("token", 0, 1), n_win * k) % np.uint64(s.vocab)
+    tok = synth.start_token(args.seed, s.vocab)
+
+    def window(i, tok):
+        toks = [int(tok)] + [int(x) for x in drafts[i * k + 1:(i + 1) * k]]
+        am, _ = B.dec_verify(dec.ctx, toks, None, k, s.kv_prefill + i * k, None)
+        return am[-1]
+
+    for i in range(args.warmup):
+        tok = window(i, tok)
+    barrier(ws)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(args.warmup, n_win):
+        tok = window(i, tok)
+    torch.cuda.synchronize()
+    secs = time.perf_counter() - t0
+    barrier(ws)
+    routed = None
+    if s.moe:  # distinct routed experts of the last window, averaged over the layers
+        routed = float(np.mean([dec.routing(l)["n_slots"] - s.n_shared for l in range(s.n_layers)]))
+    pos_mid = s.kv_prefill + k * (args.warmup + args.steps // 2)
+    bytes_win = R.algorithmic_bytes(s, pos_mid, m=k, n_routed_active=None if routed is None else round(routed))
+    per_win = max_over_ranks(secs, ws) / args.steps
+    peak, peak_kind = peaks()
+    achieved = bytes_win / per_win / 1e9
+    if rank == 0:
+        print(json.dumps({
+            "metric": METRIC, "value": whole_job_rate(args.steps * k, secs, ws), "unit": "window tokens/s",
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * per_win,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOADS[args.workload].format(L=s.n_layers), "verify": k,
+                       "step": f"one verify window of {k} tokens per dec_verify call (host waits for the argmaxes)",
+                       "mode": args.mode, "routed_experts_per_layer": routed},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                         "peak_kind": peak_kind, "traffic": None, "algorithmic_bytes_per_launch": bytes_win,
+                         "kernel": "dec_megakernel (one launch per window)"},
+        }))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -315,6 +382,7 @@ def main():
     ap.add_argument("--no-compare", action="store_true", help="skip the launch-per-op comparison")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="dense_2b", choices=sorted(WORKLOADS))
+    ap.add_argument("--verify", type=int, default=1, help="> 1: time verify windows of this many tokens (2..4)")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling captures only: fewer decoder layers (the line is then not the workload's)")
     args = ap.parse_args()
@@ -323,6 +391,8 @@ def main():
         return run_reference(args)
 
     rank, ws, local = dist_setup(args.gpus)
+    if args.verify > 1:
+        return run_verify(args, rank, ws, local)
     import torch
     import synth
     from persistent_megakernel_gb300 import build as pbuild
