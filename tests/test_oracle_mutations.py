@@ -7,6 +7,7 @@ from oracle import formats as F
 from oracle import model as M
 from oracle import ops
 import tests.test_oracle_formats as tf
+import tests.test_oracle_kv_fp8 as tk
 import tests.test_oracle_model as tm
 import tests.test_oracle_ops as to
 
@@ -69,6 +70,22 @@ def _cache_unrounded(self, l, x, pos):
         F.f64_to_bf16 = saved
 
 
+def _kv_fp64_division(x, scale):
+    return F.round_e4m3_satfinite(np.asarray(x, np.float64) / np.asarray(scale, np.float64))
+
+
+_ORIG_KV_SCALE = M.OracleModel._kv_scale
+
+
+def _kv_read_other_scale(self, l, kv, ndim):
+    # cache reads (and the prefill) take the other half's scale; the new row's write is right
+    return _ORIG_KV_SCALE(self, l, 1 - kv if ndim == 3 else kv, ndim)
+
+
+def _kv_heads_reversed(self, l, kv, ndim):
+    return self.kv_scales[l, kv][::-1].reshape((-1,) + (1,) * (ndim - 1))
+
+
 CASES = [
     ("rope sign", ops, "rope", _rope_sign, to.test_rope_pos0_identity_and_rotation_form),
     ("rope pairing", ops, "rope", _rope_interleaved, to.test_rope_pos0_identity_and_rotation_form),
@@ -90,6 +107,13 @@ CASES = [
     ("residual dropped", M.OracleModel, "attention_block", _no_residual, tm.test_dense_step_matches_loop_evaluation),
     ("cache rounding wrong", M.OracleModel, "attention_block", _cache_unrounded,
      tm.test_dense_step_matches_loop_evaluation),
+    ("kv fp8 fp64 division", F, "quantize_kv_fp8", _kv_fp64_division, tk.test_ties_saturation_and_fp32_decision),
+    ("kv fp8 read unscaled", F, "dequant_kv_fp8", lambda codes, scale: F.e4m3_to_f64(codes),
+     tk.test_lossless_fp8_cache_equals_bf16_cache),
+    ("kv fp8 keys read with value scales", M.OracleModel, "_kv_scale", _kv_read_other_scale,
+     tk.test_rescaled_keys_leave_the_step_unchanged),
+    ("kv fp8 head scales reversed", M.OracleModel, "_kv_scale", _kv_heads_reversed,
+     tk.test_lossless_fp8_cache_equals_bf16_cache),
 ]
 
 
