@@ -209,3 +209,42 @@ def test_generator_moments_and_reproducible(std):
     assert np.array_equal(a[199000:], b)               # counter-based: any slice regenerates
     v = F.bf16_to_f64(a)
     assert abs(v.mean()) < 0.01 * std and abs(v.std() / std - 1) < 0.01
+
+
+def test_generator_draws_match_splitmix64_reference():
+    # published SplitMix64 outputs for state 0 (tests/golden/splitmix64_seed0.txt)
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "splitmix64_seed0.txt")
+    want = [int(ln, 16) for ln in open(path) if ln.strip() and not ln.startswith("#")]
+    lib = synth._get()
+    assert [lib.synth_draw(0, i) for i in range(len(want))] == want
+
+
+def test_generator_normals_restate_box_muller():
+    # the normals are Box-Muller on consecutive draw pairs (restated here in Python from the
+    # definition: u1 in (0, 1], u2 in [0, 1), cos for even and sin for odd indices), rounded to
+    # bf16 by the oracle's own rounding
+    import math
+    M64 = (1 << 64) - 1
+    G = 0x9E3779B97F4A7C15
+
+    def mix(z):
+        z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & M64
+        z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & M64
+        return z ^ (z >> 31)
+
+    seed, tid, start, n = 7, synth.tensor_id("w_qkv", 3), 1001, 64
+    key = mix(mix((seed + G) & M64) ^ tid)
+    draw = lambda i: mix((key + (i + 1) * G) & M64)
+    z = []
+    for idx in range(start, start + n):
+        p = idx >> 1
+        u1 = ((draw(2 * p) >> 11) + 1) * 2.0 ** -53
+        u2 = (draw(2 * p + 1) >> 11) * 2.0 ** -53
+        r = math.sqrt(-2.0 * math.log(u1))
+        a = 6.283185307179586476925286766559 * u2
+        z.append(r * (math.sin(a) if idx & 1 else math.cos(a)))
+    z = np.array(z)
+    assert np.array_equal(synth.normal_f64(seed, tid, n, 0.0, 1.0, start=start), z)
+    got = synth.normal_bf16(seed, tid, n, 0.25, 0.02, start=start)
+    assert np.array_equal(got, F.f64_to_bf16(0.25 + 0.02 * z))
