@@ -10,6 +10,7 @@ article, section "where else the 5.9 ms goes": lane 0 of every block writes glob
 stamps to a global array; a build flag compiles it out; outputs stay bit-identical).
 
     DEC_LIB_VARIANT=trace python -m persistent_megakernel_gb300.trace [--layers N] [--steps S]
+        [--workload moe_stack]
 """
 from __future__ import annotations
 
@@ -144,6 +145,8 @@ def main(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--chrome", default="")
     ap.add_argument("--dump", default="", help="save the raw records (.npz)")
+    ap.add_argument("--workload", default="dense_2b", choices=["dense_2b", "moe_stack"],
+                    help="moe_stack: weights drawn and packed on the device")
     args = ap.parse_args(argv)
     variant = os.environ.get("DEC_LIB_VARIANT", "")
     if "trace" not in variant:
@@ -157,11 +160,16 @@ def main(argv=None):
     from .model import Decoder
     if variant == "trace":
         build.build(variant="trace")
-    s = synth.dense_2b_shape().with_(n_layers=args.layers)
-    layers = [sm.layer_weights(s, args.seed, l) for l in range(s.n_layers)]
-    head = sm.head_weights(s, args.seed)
-    kv = [sm.kv_prefill(s, args.seed, l) for l in range(s.n_layers)]
-    dec = Decoder(s, layers, head, kv=kv, capacity=s.kv_prefill + 64)
+    if args.workload == "dense_2b":
+        s = synth.dense_2b_shape().with_(n_layers=args.layers)
+        layers = [sm.layer_weights(s, args.seed, l) for l in range(s.n_layers)]
+        head = sm.head_weights(s, args.seed)
+        kv = [sm.kv_prefill(s, args.seed, l) for l in range(s.n_layers)]
+        dec = Decoder(s, layers, head, kv=kv, capacity=s.kv_prefill + 64)
+    else:
+        from tests.device_inputs import device_decoder
+        s = synth.moe_stack_shape().with_(n_layers=args.layers)
+        dec = device_decoder(s, args.seed, s.kv_prefill + 64)
     tok = synth.start_token(args.seed, s.vocab)
     for i in range(args.steps):
         clear(dec)
