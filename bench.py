@@ -22,7 +22,6 @@ import argparse
 import hashlib
 import json
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -137,25 +136,30 @@ class Clocks:
                 "reasons": reasons, "samples": len(rows)}
 
 
-def ncu_traffic(name: str, source_files):
-    """DRAM bytes per launch from the committed ncu summary, if the kernel source is unchanged."""
-    p = os.path.join(ROOT, "profiles", name)
-    if not os.path.exists(p):
-        return None
-    txt = open(p).read()
-    m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt)
-    h = re.search(r"source_sha256:\s*([0-9a-f]+)", txt)
-    if not m or not h:
-        return None
+def sources_sha256(source_files) -> str:
     sha = hashlib.sha256()
     for f in source_files:
         sha.update(open(f, "rb").read())
-    return float(m.group(1)) if sha.hexdigest() == h.group(1) else None
+    return sha.hexdigest()
+
+
+def ncu_traffic(key: str, source_files):
+    """DRAM bytes per launch of workload `key` from the committed ncu figures
+    (profiles/dram_traffic.json), if the sources they were taken on are unchanged; else None."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    rec = json.load(open(p)).get(key)
+    if not rec:
+        return None
+    return float(rec["dram_bytes_per_launch"]) if sources_sha256(source_files) == rec["source_sha256"] else None
 
 
 def kernel_sources():
+    """Every source that shapes the kernel's launches: the device code and the host runtime
+    that sets tile geometry, the op list and the workspace layout."""
     c = os.path.join(ROOT, "persistent_megakernel_gb300", "csrc")
-    return [os.path.join(c, f) for f in ("megakernel.cu", "gemv.cuh", "ptx.cuh", "dec_internal.h")]
+    return [os.path.join(c, f) for f in ("megakernel.cu", "gemv.cuh", "ptx.cuh", "dec_internal.h", "api.cpp")]
 
 
 def build_workload(seed: int, layers: int = 0):
@@ -382,7 +386,8 @@ def main():
     ap.add_argument("--no-compare", action="store_true", help="skip the launch-per-op comparison")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="dense_2b", choices=sorted(WORKLOADS))
-    ap.add_argument("--verify", type=int, default=1, help="> 1: time verify windows of this many tokens (2..4)")
+    ap.add_argument("--verify", type=int, default=1, choices=[1, 2, 3, 4],
+                    help="> 1: time verify windows of this many tokens")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling captures only: fewer decoder layers (the line is then not the workload's)")
     args = ap.parse_args()
@@ -436,7 +441,7 @@ def main():
     launch_s = secs / launches
     peak, peak_kind = peaks()
     achieved = bytes_step * (1 if args.mode == "persistent" else 1) / (secs / args.steps) / 1e9
-    traffic = ncu_traffic(f"megakernel_{args.workload}.md", kernel_sources()) if args.mode == "persistent" else None
+    traffic = ncu_traffic(args.workload, kernel_sources()) if args.mode == "persistent" and not args.layers else None
 
     # end to end through the C ABI with host buffers: token in, argmax out, every step
     K2 = min(args.steps, chain)

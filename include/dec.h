@@ -127,24 +127,64 @@ dec_status dec_init(const dec_config* cfg, void* cuda_stream, void* workspace_de
    dec_free). Tags and shapes are checked against the config; may be called repeatedly. */
 dec_status dec_load_weights(dec_ctx* ctx, const dec_tensor* tensors, int n);
 
-/* Register the KV cache: k_dev and v_dev are bf16 [n_layers][n_kv][kv_capacity][head_dim].
-   Positions below the step's pos must hold the cached (already rotated) keys and values. */
+/* Register the KV cache: k_dev and v_dev are bf16 [n_layers][n_kv][kv_capacity][head_dim],
+   caller-owned device memory, each 256-byte aligned (DEC_ERR_INVALID_ARG otherwise).
+   Positions below the step's pos must hold the cached (already rotated) keys and values; a
+   step writes its own rows at pos.. before attending over them (the Muse Spark Open
+   megakernel article, section "three bills": the layer's KV write comes before the attention
+   that reads it; the Kimi-K3 8xB300 benchmark page reads the long-context cache this way).
+   DEC_ERR_STATE for a config without attention. */
 dec_status dec_set_kv_cache(dec_ctx* ctx, void* k_dev, void* v_dev);
 
 /* One decode step of `token` at position `pos` (embedding configs), or of the given hidden
-   vector hidden_dev (bf16 [H], device; non-embedding configs, token ignored).
+   vector hidden_dev (bf16 [H], device, 16-byte aligned; non-embedding configs, token ignored):
+   the whole step of the file header in one persistent launch (Kog, "3k tokens/s per
+   request", section on the monokernel: embedding row, every layer, LM head and greedy argmax
+   without returning to the host; Muse Spark Open megakernel article, "the baseline nobody
+   benchmarked", for the launch count it removes).
    Writes the new key/value at pos. logits_dev (nullable, fp32 [V], device) receives the
-   logits; argmax_host (nullable) receives the greedy token and makes the call wait. */
+   logits; argmax_host (nullable) receives the greedy token (lowest index among equal
+   maxima) and makes the call wait and check the device status word.
+   Errors: DEC_ERR_CAPACITY when pos >= kv_capacity or token >= vocab, DEC_ERR_INVALID_ARG on
+   a missing or misaligned hidden_dev, DEC_ERR_STATE while a device error is pending. */
 dec_status dec_step(dec_ctx* ctx, int32_t token, const void* hidden_dev, int32_t pos,
                     float* logits_dev, int32_t* argmax_host);
+
+/* One decoder layer on its own, from and to bf16 hidden vectors (device memory the caller
+   owns, 16-byte aligned): h_out[m][H] = layer `layer` applied to h_in[m][H] for the m tokens at
+   positions pos .. pos + m - 1 (1 <= m <= max_verify), with the layer's own weights and KV cache
+   slice (its rows at pos .. are written, as in a step). The layer runs exactly as inside a
+   step (pre-norm attention block, then the dense SwiGLU or the MoE block of the file header;
+   Kog, "3k tokens/s per request", for the decoder layer; Ling-3.0-flash on DGX Spark, "model
+   and baseline configuration", for the MoE block); only its result is rounded to bf16 where it
+   leaves the library. MoE layers: topk_idx_dev (nullable, int32 [m][top_k]) receives each
+   token's routed experts, best first (lowest index among equal logits), and topk_w_dev
+   (nullable, fp32 [m][top_k]) their weights, the softmax over the selected router logits.
+   Ordered on the context's stream; does not wait. Errors: DEC_ERR_SHAPE for a layer outside
+   the config, DEC_ERR_CAPACITY past kv_capacity, DEC_ERR_STATE for top-k outputs on a layer
+   without MoE, missing weights or a pending device error, DEC_ERR_INVALID_ARG on null or
+   misaligned hidden pointers. */
+dec_status dec_run_layer(dec_ctx* ctx, int layer, const void* h_in, int m, int32_t pos, void* h_out,
+                         int32_t* topk_idx_dev, float* topk_w_dev);
+
+/* The final norm (when the config has one) and the LM head on their own, from given bf16
+   hidden vectors h_in[m][H] (device, 16-byte aligned): logits_dev (nullable, fp32 [m][V],
+   device; NULL keeps them in the workspace) and argmax_host (nullable, int32 [m], host: the
+   greedy token of each row, lowest index among equal maxima; makes the call wait and check the
+   device status word). Same kernel as a step's LM head: bf16, or FP8 e4m3 codes times a per-row
+   scale (Ling-3.0-flash on DGX Spark, section "optimisation 2: online FP8 LM head").
+   DEC_ERR_STATE for a config without an LM head. */
+dec_status dec_lm_head(dec_ctx* ctx, const void* h_in, int m, float* logits_dev, int32_t* argmax_host);
 
 /* n greedy steps chained on the device: step i feeds the argmax of step i-1 (the first one
    feeds `token`) at position pos + i. No host synchronisation between steps.
    tokens_dev (nullable, int32 [n], device) receives the n generated tokens. */
 dec_status dec_generate(dec_ctx* ctx, int32_t token, int32_t pos, int n, int32_t* tokens_dev);
 
-/* Verify window: tokens_host[i] (i < k <= max_verify) is fed at pos + i in one pass, each
-   seeing positions 0..pos+i. logits_dev (nullable, fp32 [k][V]); argmax_host (nullable,
+/* Verify window (Ling-3.0-flash on DGX Spark, section "optimisation 3": the MTP verify pass
+   that scores the drafted tokens in one forward and keeps the correct prefix):
+   tokens_host[i] (i < k <= max_verify) is fed at pos + i in one pass, each
+   seeing positions 0..pos+i (causal inside the window); weights are streamed once for all k. logits_dev (nullable, fp32 [k][V]); argmax_host (nullable,
    [k]); n_accepted (nullable): the longest j with tokens[i+1] == argmax[i] for all i < j,
    plus one (the model's own next token). Non-embedding configs pass hidden_dev (bf16 [k][H])
    and tokens_host may be NULL. Keys/values of all k positions are written. */
@@ -175,7 +215,9 @@ dec_status dec_debug_buffers(dec_ctx* ctx, const uint64_t** hidden, const uint64
 dec_status dec_trace_buffer(dec_ctx* ctx, const uint64_t** records, int* n_ctas, int* n_ops);
 
 /* Clear a sticky device error: zeroes the whole workspace (step counters, status word and
-   every handed-over activation) after waiting for the stream. Weights and KV cache are kept. */
+   every handed-over activation) after waiting for the stream. Weights and KV cache are kept.
+   The bounded waits it recovers from are this library's own failure detection (the pages'
+   kernels spin on flags without a limit; Muse Spark Open megakernel article, "three bills"). */
 dec_status dec_reset(dec_ctx* ctx);
 
 /* Wait for the context's stream; returns a sticky device error if one was raised. */
@@ -205,10 +247,11 @@ int dec_last_launch_count(dec_ctx* ctx);
    Its scratch (step state, argmax partials, status) is a static device array of 64 KiB in
    the library, which every GPU that loads the library keeps until the process exits; a call
    needs about 256 * 5 + 32 * (SM count) bytes of it and returns DEC_ERR_CAPACITY beyond that.
-   The first call on a device looks up the array's device address, so make it before any
-   stream capture. Every call clears and reuses the same array: calls that overlap on the GPU
-   (other streams, other threads) race, so serialise them. Waits for the result
-   (synchronises the stream) and returns a device error if the kernel raised one.
+   The first call on a device looks up the array's device address. The call synchronises the
+   stream it is given (it waits for the result), so it must not be issued on a stream that is
+   being captured. Every call clears and reuses the same array: calls that overlap on the GPU
+   (other streams, other threads) race, so serialise them. Returns a device error if the
+   kernel raised one.
    m: 1..4; hidden a multiple of 64. */
 dec_status dec_lm_head_noalloc(int hidden, int vocab, dec_dtype dtype, int m, float rms_eps, const void* hidden_dev,
                                const void* final_norm_dev, const void* w_values_dev, const void* w_scales_dev,

@@ -36,7 +36,8 @@ DEC_MODE_PER_OP_GRAPH = 2
 # every symbol include/dec.h declares
 EXPORTS = ("dec_workspace_bytes", "dec_init", "dec_load_weights", "dec_set_kv_cache", "dec_step", "dec_generate",
            "dec_verify", "dec_debug_buffers", "dec_reset", "dec_sync", "dec_last_launch_count", "dec_last_error",
-           "dec_free", "dec_packed_bytes", "dec_pack", "dec_pack_pair", "dec_pack_device", "dec_pack_pair_device", "dec_trace_buffer", "dec_lm_head_noalloc", "dec_debug_drop_op")
+           "dec_free", "dec_packed_bytes", "dec_pack", "dec_pack_pair", "dec_pack_device", "dec_pack_pair_device", "dec_trace_buffer", "dec_lm_head_noalloc", "dec_debug_drop_op",
+           "dec_run_layer", "dec_lm_head")
 
 
 class DecConfig(ctypes.Structure):
@@ -76,6 +77,8 @@ def lib():
             "dec_set_kv_cache": (I, [P, P, P]),
             "dec_step": (I, [P, ctypes.c_int32, P, ctypes.c_int32, P, P]),
             "dec_generate": (I, [P, ctypes.c_int32, ctypes.c_int32, I, P]),
+            "dec_run_layer": (I, [P, I, P, I, ctypes.c_int32, P, P, P]),
+            "dec_lm_head": (I, [P, P, I, P, P]),
             "dec_verify": (I, [P, P, P, I, ctypes.c_int32, P, P, P]),
             "dec_debug_buffers": (I, [P, ctypes.POINTER(P), ctypes.POINTER(P), ctypes.POINTER(P)]),
             "dec_trace_buffer": (I, [P, ctypes.POINTER(P), ctypes.POINTER(I), ctypes.POINTER(I)]),
@@ -145,6 +148,16 @@ def dec_step(ctx: int, token: int, hidden, pos: int, logits=None, want_argmax=Tr
     am = ctypes.c_int32(-1)
     check(lib().dec_step(ctx, token, _p(hidden), pos, _p(logits), ctypes.byref(am) if want_argmax else None))
     return am.value if want_argmax else None
+
+
+def dec_run_layer(ctx: int, layer: int, h_in, m: int, pos: int, h_out, topk_idx=None, topk_w=None) -> None:
+    check(lib().dec_run_layer(ctx, layer, _p(h_in), m, pos, _p(h_out), _p(topk_idx), _p(topk_w)))
+
+
+def dec_lm_head(ctx: int, h_in, m: int, logits=None, want_argmax=True):
+    am = (ctypes.c_int32 * 4)()
+    check(lib().dec_lm_head(ctx, _p(h_in), m, _p(logits), am if want_argmax else None))
+    return list(am)[:m] if want_argmax else None
 
 
 def dec_generate(ctx: int, token: int, pos: int, n: int, tokens_out=None) -> None:

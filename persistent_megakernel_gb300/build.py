@@ -6,6 +6,7 @@ only when a source or header is newer than the library.
 from __future__ import annotations
 
 import glob
+import hashlib
 import os
 import shutil
 import subprocess
@@ -51,10 +52,29 @@ def _stale(lib: str) -> bool:
     return any(os.path.getmtime(p) > t for p in deps)
 
 
+def sources_sha256() -> str:
+    """sha256 over every source and header the library is built from, in a fixed order."""
+    sha = hashlib.sha256()
+    for p in sorted(sources() + glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh"))) + [
+            os.path.join(INCLUDE, "dec.h")]:
+        sha.update(os.path.basename(p).encode())
+        sha.update(open(p, "rb").read())
+    return sha.hexdigest()
+
+
+def _log(msg: str) -> None:
+    # stderr: a bench prints its one result line on stdout
+    sys.stderr.write(f"[libdec build] {msg}\n")
+    sys.stderr.flush()
+
+
 def build(force: bool = False, verbose: bool = False, extra_nvcc=(), variant: str = "", defines=()) -> str:
-    """Build libdec.so (or libdec_<variant>.so with the variant's -D flags plus `defines`)."""
+    """Build libdec.so (or libdec_<variant>.so with the variant's -D flags plus `defines`).
+    Prints one line saying whether it compiled from source or found the library up to date,
+    with the sha256 of the sources."""
     lib = lib_path(variant)
     if not force and not _stale(lib):
+        _log(f"{os.path.basename(lib)} up to date (sources sha256 {sources_sha256()[:16]}), not recompiled")
         return lib
     defs = VARIANTS.get(variant, []) + list(defines)
     nvcc = _nvcc()
@@ -89,6 +109,8 @@ def build(force: bool = False, verbose: bool = False, extra_nvcc=(), variant: st
     if r.returncode != 0:
         raise RuntimeError("linking libdec.so failed:\n" + r.stdout)
     os.replace(tmp, lib)
+    _log(f"{os.path.basename(lib)} compiled from source: {len(objs)} translation units, sources sha256 "
+         f"{sources_sha256()[:16]}, nvcc {' '.join(ARCH)} -O3 {' '.join(defs)}".rstrip())
     return lib
 
 

@@ -61,8 +61,10 @@ struct LayerW {
   const void* edn_s = nullptr;
 };
 
+constexpr int kMaxSubOps = 8;  // ops of one layer (at most 7) or of the LM head alone
+
 struct Layout {  // byte offsets into the workspace
-  size_t state, status, tickets, ctr, ops, hs, qkv, attn_out, hbuf, rlogits, route, eh, part, logits, am_val, am_idx,
+  size_t state, status, tickets, ctr, ops, subops, hs, qkv, attn_out, hbuf, rlogits, route, eh, part, logits, am_val, am_idx,
       am_out, trace, total;
   int n_ops, n_tickets, n_ctas, ns_max, slot_bytes, act_bytes, exp_stage_all;
 };
@@ -222,6 +224,7 @@ bool compute_layout(const dec_config* c, Layout& L, std::string& why) {
   L.tickets = take((size_t)L.n_tickets * 4);
   L.ctr = take((size_t)(std::max(1, L.n_ops) + (c->n_q ? nl * c->n_kv : 0)) * 4);
   L.ops = take((size_t)std::max(1, L.n_ops) * sizeof(OpDesc));
+  L.subops = take((size_t)kMaxSubOps * sizeof(OpDesc));  // a layer or the LM head run on its own
   // activations handed between CTAs are tagged 8-byte words (see ptx.cuh), one buffer per
   // layer so that no word is written twice in a step
   L.hs = take((size_t)(2 * nl + 1) * M * H * 8);
@@ -276,54 +279,66 @@ T* wsp(dec_ctx* c, size_t off) {
   return reinterpret_cast<T*>(c->ws + off);
 }
 
-dec_status check_weights(dec_ctx* c) {
+dec_status check_layer(dec_ctx* c, int l) {
   const dec_config& g = c->cfg;
-  for (int l = 0; l < g.n_layers; ++l) {
-    const LayerW& w = c->layers[l];
-    if (g.n_q && (!w.attn_norm || !w.wqkv || !w.wo)) return fail(DEC_ERR_STATE, "layer %d: attention weights missing", l);
-    if ((g.ffn || g.n_experts) && !w.ffn_norm) return fail(DEC_ERR_STATE, "layer %d: ffn_norm missing", l);
-    if (g.ffn && (!w.wgateup || !w.wdown)) return fail(DEC_ERR_STATE, "layer %d: dense FFN weights missing", l);
-    if (g.n_experts && (!w.wrouter || !w.egu_v || !w.egu_s || !w.edn_v || !w.edn_s))
-      return fail(DEC_ERR_STATE, "layer %d: MoE weights missing", l);
-  }
-  if (g.embedding && !c->embed) return fail(DEC_ERR_STATE, "embedding missing");
-  if (g.vocab && (!c->lm_v || (g.final_norm && !c->final_norm))) return fail(DEC_ERR_STATE, "LM head missing");
-  if (g.vocab && g.lm_head_dtype == DEC_FP8_E4M3_ROWSCALE && !c->lm_s) return fail(DEC_ERR_STATE, "LM head scales missing");
+  const LayerW& w = c->layers[l];
+  if (g.n_q && (!w.attn_norm || !w.wqkv || !w.wo)) return fail(DEC_ERR_STATE, "layer %d: attention weights missing", l);
+  if ((g.ffn || g.n_experts) && !w.ffn_norm) return fail(DEC_ERR_STATE, "layer %d: ffn_norm missing", l);
+  if (g.ffn && (!w.wgateup || !w.wdown)) return fail(DEC_ERR_STATE, "layer %d: dense FFN weights missing", l);
+  if (g.n_experts && (!w.wrouter || !w.egu_v || !w.egu_s || !w.edn_v || !w.edn_s))
+    return fail(DEC_ERR_STATE, "layer %d: MoE weights missing", l);
   if (g.n_q && (!c->kc || !c->vc)) return fail(DEC_ERR_STATE, "KV cache not set");
   return DEC_OK;
 }
 
-void build_ops(dec_ctx* c) {
+dec_status check_head(dec_ctx* c) {
   const dec_config& g = c->cfg;
-  const Layout& L = c->lay;
-  const int C = L.n_ctas, M = g.max_verify, H = g.hidden;
-  const int qkv_rows = g.n_q ? (g.n_q + 2 * g.n_kv) * kHeadDim : 0;
-  uint64_t* hs = wsp<uint64_t>(c, L.hs);
-  std::vector<OpDesc>& ops = c->ops;
-  ops.clear();
-  int ticket = 0;
-  // x of the next block: the call's input first, then the hidden-stream entry last written
-  int xsrc = g.embedding ? X_EMBED : X_HIDDEN_IN, x_idx = 0;
-  // dependencies for builds that gate reads on arrival counts (DEC_POLL_DATA=0; by default the
-  // kernel polls the tagged inputs directly): every op announces its completion on its own
-  // counter, and an op waits for the counter of the op that produced its newest input (ops run
-  // in list order in every CTA, so older inputs are complete too)
-  int prev = -1;
-  auto blank = [&](int type) {
+  if (g.vocab && (!c->lm_v || (g.final_norm && !c->final_norm))) return fail(DEC_ERR_STATE, "LM head missing");
+  if (g.vocab && g.lm_head_dtype == DEC_FP8_E4M3_ROWSCALE && !c->lm_s) return fail(DEC_ERR_STATE, "LM head scales missing");
+  return DEC_OK;
+}
+
+dec_status check_weights(dec_ctx* c) {
+  const dec_config& g = c->cfg;
+  for (int l = 0; l < g.n_layers; ++l) {
+    const dec_status st = check_layer(c, l);
+    if (st != DEC_OK) return st;
+  }
+  if (g.embedding && !c->embed) return fail(DEC_ERR_STATE, "embedding missing");
+  return check_head(c);
+}
+
+constexpr int kLmHeadTicket = 0;  // tickets: the LM head's argmax, then the step end
+constexpr int kStepTicket = 1;
+
+// Op-list builder: the ops of a layer or of the LM head, appended to a list. The state
+// carries what the next block reads (its input's source and hidden-stream entry) and the op
+// producing it (for the counted-read build option).
+struct ListBuilder {
+  dec_ctx* c;
+  std::vector<OpDesc>& ops;
+  int xsrc, x_idx, prev;
+
+  ListBuilder(dec_ctx* c_, std::vector<OpDesc>& ops_, int xsrc_) : c(c_), ops(ops_), xsrc(xsrc_), x_idx(0), prev(-1) {}
+
+  OpDesc blank(int type) const {
     OpDesc o;
     std::memset(&o, 0, sizeof(o));
     o.type = type;
     o.ctr = (int)ops.size();
     o.wait_ctr = prev;
-    o.wait_n = C;
+    o.wait_n = c->lay.n_ctas;
     o.aux_ctr = -1;
     o.xsrc = xsrc;
     o.x_idx = x_idx;
     o.x_src = c->embed;
     o.slot1 = -1;
     return o;
-  };
-  auto geom = [&](OpDesc& o) {
+  }
+
+  void geom(OpDesc& o) const {
+    const Layout& L = c->lay;
+    const int M = c->cfg.max_verify;
     tile_geometry(o.wtype, o.K, o.pair, L.slot_bytes, M, o.R, o.Kc, o.unit);
     // rows too wide for one slot (or for activations in registers): split the columns across
     // the CTA's warps instead of its rows (bf16 / FP8 matrices without expert slots)
@@ -341,10 +356,19 @@ void build_ops(dec_ctx* c) {
         o.R = r / o.unit * o.unit;
       }
     }
-  };
-  auto hs_at = [&](int idx) { return hs + (size_t)idx * M * H; };  // tagged [Mmax][H]
+  }
 
-  for (int l = 0; l < g.n_layers; ++l) {
+  uint64_t* hs_at(int idx) const {  // tagged [Mmax][H]
+    return wsp<uint64_t>(c, c->lay.hs) + (size_t)idx * c->cfg.max_verify * c->cfg.hidden;
+  }
+
+  // The ops of decoder layer l: attention block (QKV, attention, o-proj), then the dense FFN
+  // (gate/up, down) or the MoE FFN (router, shared and routed gate/up, expert down).
+  void layer(int l) {
+    const dec_config& g = c->cfg;
+    const Layout& L = c->lay;
+    const int M = g.max_verify, H = g.hidden;
+    const int qkv_rows = g.n_q ? (g.n_q + 2 * g.n_kv) * kHeadDim : 0;
     const LayerW& w = c->layers[l];
     if (g.n_q) {
       OpDesc q = blank(OP_QKV);
@@ -503,25 +527,37 @@ void build_ops(dec_ctx* c) {
       x_idx = 2 * l + 2;
     }
   }
-  if (g.vocab) {
-    OpDesc h = blank(OP_LMHEAD);
-    h.wtype = g.lm_head_dtype == DEC_FP8_E4M3_ROWSCALE ? W_FP8 : W_BF16;
-    h.N = g.vocab;
-    h.K = H;
-    h.norm = g.final_norm ? 1 : 0;
-    h.gain = static_cast<const uint16_t*>(c->final_norm);
-    h.w = c->lm_v;
-    h.ws = c->lm_s;
-    h.logits = wsp<float>(c, L.logits);
-    h.ticket = ticket++;
-    geom(h);
-    ops.push_back(h);
-  }
 
-  KParams& k = c->kp;
+  // The final norm and the LM head (logits to `logits`, argmax through the LM-head ticket).
+  void head(float* logits) {
+    const dec_config& g = c->cfg;
+    const int H = g.hidden;
+    if (g.vocab) {
+      OpDesc h = blank(OP_LMHEAD);
+      h.wtype = g.lm_head_dtype == DEC_FP8_E4M3_ROWSCALE ? W_FP8 : W_BF16;
+      h.N = g.vocab;
+      h.K = H;
+      h.norm = g.final_norm ? 1 : 0;
+      h.gain = static_cast<const uint16_t*>(c->final_norm);
+      h.w = c->lm_v;
+      h.ws = c->lm_s;
+      h.logits = logits;
+      h.ticket = kLmHeadTicket;
+      geom(h);
+      ops.push_back(h);
+    }
+  }
+};
+
+// Kernel parameters of an op list of n_ops ops at byte offset ops_off of the workspace.
+void fill_params(dec_ctx* c, KParams& k, size_t ops_off, int n_ops) {
+  const dec_config& g = c->cfg;
+  const Layout& L = c->lay;
+  const int M = g.max_verify, H = g.hidden, C = L.n_ctas;
+  const int qkv_rows = g.n_q ? (g.n_q + 2 * g.n_kv) * kHeadDim : 0;
   std::memset(&k, 0, sizeof(k));
-  k.ops = wsp<OpDesc>(c, L.ops);
-  k.n_ops = (int)ops.size();
+  k.ops = wsp<OpDesc>(c, ops_off);
+  k.n_ops = n_ops;
   k.op_begin = 0;
   k.op_end = k.n_ops;
   k.n_ctas = C;
@@ -552,11 +588,21 @@ void build_ops(dec_ctx* c) {
   k.am_val = wsp<float>(c, L.am_val);
   k.am_idx = wsp<int32_t>(c, L.am_idx);
   k.am_out = wsp<int32_t>(c, L.am_out);
-  k.step_ticket = ticket++;
-  k.hs = hs;
+  k.step_ticket = kStepTicket;
+  k.hs = wsp<uint64_t>(c, L.hs);
 #ifdef DEC_TRACE
   k.trace = wsp<uint64_t>(c, L.trace);
 #endif
+}
+
+// The whole step: every layer, then the LM head.
+void build_ops(dec_ctx* c) {
+  const dec_config& g = c->cfg;
+  c->ops.clear();
+  ListBuilder b(c, c->ops, g.embedding ? X_EMBED : X_HIDDEN_IN);
+  for (int l = 0; l < g.n_layers; ++l) b.layer(l);
+  if (g.vocab) b.head(wsp<float>(c, c->lay.logits));
+  fill_params(c, c->kp, c->lay.ops, (int)c->ops.size());
 }
 
 dec_status prepare(dec_ctx* c) {
@@ -576,9 +622,12 @@ dec_status prepare(dec_ctx* c) {
   return DEC_OK;
 }
 
-dec_status launch_step(dec_ctx* c) {
-  KParams k = c->kp;
-  const dec_mode mode = c->cfg.mode;
+// Launch an op list in the context's mode. The CUDA graph of the per-op-graph mode holds the
+// whole step's list; other lists (a layer or the LM head on its own) run as plain per-op launches
+// in that mode.
+dec_status launch_list(dec_ctx* c, const KParams& k, bool whole_step) {
+  dec_mode mode = c->cfg.mode;
+  if (mode == DEC_MODE_PER_OP_GRAPH && !whole_step) mode = DEC_MODE_PER_OP;
   if (mode == DEC_MODE_PERSISTENT) {
     CUDA_TRY(dec_launch_megakernel(&k, 1, c->stream));
     c->last_launches = 1;
@@ -605,8 +654,8 @@ dec_status launch_step(dec_ctx* c) {
     c->last_launches = k.n_ops;
     return DEC_OK;
   }
-  const int drop = c->drop_op;
-  c->drop_op = -1;
+  const int drop = whole_step ? c->drop_op : -1;
+  if (whole_step) c->drop_op = -1;
   int launched = 0;
   for (int i = 0; i < k.n_ops; ++i) {
     if (i == drop) continue;  // injected failure: this op's outputs are never written
@@ -676,7 +725,7 @@ dec_status run_call(dec_ctx* c, int32_t pos, int m, const int32_t* tokens, const
   if (st != DEC_OK) return st;
   st = write_state(c, pos, m, tokens, hidden, 0, nullptr);
   if (st != DEC_OK) return st;
-  st = launch_step(c);
+  st = launch_list(c, c->kp, true);
   if (st != DEC_OK) return st;
   if (logits_dev && c->cfg.vocab)
     CUDA_TRY(cudaMemcpyAsync(logits_dev, c->ws + c->lay.logits, (size_t)m * c->cfg.vocab * 4, cudaMemcpyDeviceToDevice,
@@ -687,6 +736,29 @@ dec_status run_call(dec_ctx* c, int32_t pos, int m, const int32_t* tokens, const
   }
   return DEC_OK;
 }
+
+// Run an op list of its own (a layer or the LM head) from the given hidden vectors: the list
+// goes to the workspace's second op region and runs in the context's mode. argmax_host
+// (nullable) receives the list's argmaxes and makes the call wait and check the status word.
+dec_status run_sub(dec_ctx* c, const std::vector<OpDesc>& ops, int32_t pos, int m, const void* hidden,
+                   int32_t* argmax_host) {
+  if ((int)ops.size() > kMaxSubOps) return fail(DEC_ERR_STATE, "%zu ops exceed the sub-list region", ops.size());
+  CUDA_TRY(cudaMemcpyAsync(c->ws + c->lay.subops, ops.data(), ops.size() * sizeof(OpDesc), cudaMemcpyHostToDevice,
+                           c->stream));
+  KParams k;
+  fill_params(c, k, c->lay.subops, (int)ops.size());
+  dec_status st = write_state(c, pos, m, nullptr, hidden, 0, nullptr);
+  if (st != DEC_OK) return st;
+  st = launch_list(c, k, false);
+  if (st != DEC_OK) return st;
+  if (argmax_host) {
+    CUDA_TRY(cudaMemcpyAsync(argmax_host, c->ws + c->lay.am_out, (size_t)m * 4, cudaMemcpyDeviceToHost, c->stream));
+    return read_status(c);
+  }
+  return DEC_OK;
+}
+
+bool aligned16(const void* q) { return reinterpret_cast<uintptr_t>(q) % 16 == 0; }
 
 }  // namespace
 
@@ -851,6 +923,48 @@ dec_status dec_verify(dec_ctx* c, const int32_t* tokens_host, const void* hidden
   return DEC_OK;
 }
 
+dec_status dec_run_layer(dec_ctx* c, int layer, const void* h_in, int m, int32_t pos, void* h_out,
+                         int32_t* topk_idx_dev, float* topk_w_dev) {
+  if (!c) return fail(DEC_ERR_INVALID_ARG, "null context");
+  const dec_config& g = c->cfg;
+  if (c->sticky) return fail(DEC_ERR_STATE, "a device error is pending (code %d): call dec_reset", (int)c->sticky_code);
+  if (layer < 0 || layer >= g.n_layers) return fail(DEC_ERR_SHAPE, "layer %d outside 0..%d", layer, g.n_layers - 1);
+  if (m < 1 || m > g.max_verify) return fail(DEC_ERR_INVALID_ARG, "window of %d tokens (max_verify %d)", m, g.max_verify);
+  if (!h_in || !aligned16(h_in) || !h_out || !aligned16(h_out))
+    return fail(DEC_ERR_INVALID_ARG, "h_in and h_out must be non-null and 16-byte aligned");
+  if ((topk_idx_dev || topk_w_dev) && !g.n_experts) return fail(DEC_ERR_STATE, "top-k outputs need a MoE layer");
+  if (pos < 0) return fail(DEC_ERR_INVALID_ARG, "negative position");
+  if (g.n_q && (long long)pos + m > g.kv_capacity)
+    return fail(DEC_ERR_CAPACITY, "positions %d..%d exceed kv_capacity %d", pos, pos + m - 1, g.kv_capacity);
+  dec_status st = check_layer(c, layer);
+  if (st != DEC_OK) return st;
+  std::vector<OpDesc> ops;
+  ListBuilder b(c, ops, X_HIDDEN_IN);
+  b.layer(layer);
+  ops.back().y_bf16 = static_cast<uint16_t*>(h_out);  // the layer's last op writes its residual output
+  for (OpDesc& o : ops)
+    if (o.type == OP_ROUTER) {
+      o.topk_idx_out = topk_idx_dev;
+      o.topk_w_out = topk_w_dev;
+    }
+  return run_sub(c, ops, pos, m, h_in, nullptr);
+}
+
+dec_status dec_lm_head(dec_ctx* c, const void* h_in, int m, float* logits_dev, int32_t* argmax_host) {
+  if (!c) return fail(DEC_ERR_INVALID_ARG, "null context");
+  const dec_config& g = c->cfg;
+  if (c->sticky) return fail(DEC_ERR_STATE, "a device error is pending (code %d): call dec_reset", (int)c->sticky_code);
+  if (!g.vocab) return fail(DEC_ERR_STATE, "config has no LM head");
+  if (m < 1 || m > g.max_verify) return fail(DEC_ERR_INVALID_ARG, "window of %d tokens (max_verify %d)", m, g.max_verify);
+  if (!h_in || !aligned16(h_in)) return fail(DEC_ERR_INVALID_ARG, "h_in must be non-null and 16-byte aligned");
+  dec_status st = check_head(c);
+  if (st != DEC_OK) return st;
+  std::vector<OpDesc> ops;
+  ListBuilder b(c, ops, X_HIDDEN_IN);
+  b.head(logits_dev ? logits_dev : wsp<float>(c, c->lay.logits));
+  return run_sub(c, ops, 0, m, h_in, argmax_host);
+}
+
 dec_status dec_generate(dec_ctx* c, int32_t token, int32_t pos, int n, int32_t* tokens_dev) {
   if (!c) return fail(DEC_ERR_INVALID_ARG, "null context");
   if (n < 0) return fail(DEC_ERR_INVALID_ARG, "negative step count");
@@ -866,7 +980,7 @@ dec_status dec_generate(dec_ctx* c, int32_t token, int32_t pos, int n, int32_t* 
   if (st != DEC_OK) return st;
   int launches = 0;
   for (int i = 0; i < n; ++i) {
-    st = launch_step(c);
+    st = launch_list(c, c->kp, true);
     if (st != DEC_OK) return st;
     launches += c->last_launches;
   }

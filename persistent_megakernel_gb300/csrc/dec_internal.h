@@ -78,6 +78,10 @@ struct OpDesc {
   uint16_t* vc;                       // this layer's value cache bf16 [n_kv][cap][128]
   int32_t* route;                     // this layer's RouteBlock
   uint64_t* eh;                       // this layer's expert hidden, tagged [slots][Mmax][I]
+  uint16_t* y_bf16;                   // residual ops: also store the output rounded to bf16 here,
+                                      // [Mmax][H] (a layer run on its own hands its result back)
+  int32_t* topk_idx_out;              // router: also store each token's top-k experts, [m][top_k]
+  float* topk_w_out;                  // router: and their routing weights, [m][top_k]
 };
 
 struct RouteBlock {

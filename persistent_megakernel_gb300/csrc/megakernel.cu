@@ -23,6 +23,8 @@
 #include <cuda_runtime.h>
 #include <math.h>
 
+#include <mutex>
+
 #include "../../include/dec.h"
 #include "dec_internal.h"
 #include "gemv.cuh"
@@ -821,12 +823,17 @@ struct Consumer {
   __device__ __forceinline__ void tile_log(int) {}
 #endif
 
-  // Arrive at ticket t (n arrivals per step); true in the last arrival (all consumers agree).
+  // Arrive at ticket t (n arrivals per use); true in the last arrival (all consumers agree).
+  // The last arrival sets the ticket back to zero: its next use comes in a later launch, after
+  // every arrival of this one, so a call that skips the op holding a ticket (a layer or the LM
+  // head run on its own) leaves no count behind.
   __device__ bool ticket(int t, int n) {
     consumer_sync();
     if (tid == 0) {
       const uint32_t old = atom_add_acq_rel(&p.tickets[t], 1u);
-      s.flags[kFlagTicket] = (old == (epoch + 1u) * (uint32_t)n - 1u) ? 1 : 0;
+      const bool last = old == (uint32_t)n - 1u;
+      if (last) atomicExch(&p.tickets[t], 0u);
+      s.flags[kFlagTicket] = last ? 1 : 0;
     }
     consumer_sync();
     return s.flags[kFlagTicket] != 0;
@@ -936,6 +943,13 @@ struct Consumer {
       }
     }
     return ok;
+  }
+
+  // Residual output x_m[row] = v of a residual op (o-proj, down, expert down): the tagged word,
+  // and its bf16 rounding where the caller takes the result (a layer run on its own).
+  __device__ __forceinline__ void put_x(const OpDesc& op, int m, int row, float v) {
+    st_tagged(op.x_out + (size_t)m * p.H + row, v, tag);
+    if (op.y_bf16) op.y_bf16[(size_t)m * p.H + row] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
   }
 
   __device__ __forceinline__ const uint16_t* x_bf16(const OpDesc& op, int m) const {
@@ -1146,6 +1160,11 @@ struct Consumer {
     if (blockIdx.x == 0) {  // a copy in global memory for inspection
       const int* src = reinterpret_cast<const int*>(rb);
       for (int i = tid; i < (int)(sizeof(RouteBlock) / 4); i += kConsumerThreads) op.route[i] = src[i];
+      // the caller's copies of the selection (a layer run on its own)
+      for (int i = tid; i < M * k; i += kConsumerThreads) {
+        if (op.topk_idx_out) op.topk_idx_out[i] = rb->topk[i / k][i % k];
+        if (op.topk_w_out) op.topk_w_out[i] = rb->topk_w[i / k][i % k];
+      }
     }
     return true;
   }
@@ -1199,7 +1218,7 @@ struct Consumer {
           break;
         case OP_OPROJ:
         case OP_DOWN:
-          if (mine) st_tagged(op.x_out + (size_t)m * p.H + t.r0 + i, xres[(t.r0 + i - a) * M + m] + v, tag);
+          if (mine) put_x(op, m, t.r0 + i, xres[(t.r0 + i - a) * M + m] + v);
           break;
         case OP_GATEUP:
         case OP_SHARED_GATEUP:
@@ -1297,7 +1316,7 @@ struct Consumer {
       const int r = t / M, m = t % M;
       const float v = rowsum(r, m);
       if (op.type == OP_OPROJ || op.type == OP_DOWN)
-        st_tagged(op.x_out + (size_t)m * p.H + a + r, xres[t] + v, tag);
+        put_x(op, m, a + r, xres[t] + v);
       else
         st_tagged(op.out + (size_t)m * op.N + a + r, v, tag);
     }
@@ -1481,7 +1500,7 @@ struct Consumer {
     if (op.type == OP_EXP_DOWN) {
       for (int t = tid; t < (g.b - g.a) * M; t += kConsumerThreads) {
         const int i = t / M, m = t % M;
-        st_tagged(op.x_out + (size_t)m * p.H + g.a + i, g.xres[t] + g.accd[t], tag);
+        put_x(op, m, g.a + i, g.xres[t] + g.accd[t]);
       }
     }
     if (op.type == OP_ROUTER) {
@@ -1906,14 +1925,28 @@ __global__ void __launch_bounds__(kThreads, 1) dec_megakernel(const __grid_const
 }  // namespace decimpl
 
 // ------------------------------------------------------------------ host launch
+namespace {
+// Largest dynamic shared-memory size the kernel has been allowed on each device so far: the
+// attribute belongs to the device that was current when it was set, so every device gets its
+// own, and host threads launching at once take the lock.
+constexpr int kMaxDevices = 64;
+std::mutex g_attr_mu;
+size_t g_attr_bytes[kMaxDevices] = {};
+}  // namespace
+
 extern "C" cudaError_t dec_launch_megakernel(const decimpl::KParams* kp, int cooperative, cudaStream_t stream) {
   using namespace decimpl;
   const size_t smem = (size_t)kConsumerWarps * kStages * kp->slot_bytes + kp->act_bytes + kCommonBytes;
-  static size_t attr_bytes = 0;  // largest dynamic size the kernel has been allowed so far
-  if (smem > attr_bytes) {
-    cudaError_t e = cudaFuncSetAttribute(dec_megakernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr_bytes = smem;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  {
+    std::lock_guard<std::mutex> lock(g_attr_mu);
+    if (dev < 0 || dev >= kMaxDevices || smem > g_attr_bytes[dev]) {
+      e = cudaFuncSetAttribute(dec_megakernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      if (dev >= 0 && dev < kMaxDevices) g_attr_bytes[dev] = smem;
+    }
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)kp->n_ctas);

@@ -220,6 +220,25 @@ class Decoder:
         k = k if k is not None else len(tokens)
         return B.dec_verify(self.ctx, tokens, hidden, k, pos, self.logits)
 
+    def run_layer(self, layer: int, h_in: torch.Tensor, pos: int, topk: bool = False):
+        """One decoder layer on its own: bf16 [m, H] in (2-byte elements on the device), bf16
+        [m, H] out; with topk (MoE layers) also the [m, top_k] expert ids and weights."""
+        m = h_in.shape[0]
+        h_out = torch.empty_like(h_in)
+        s = self.shape
+        idx = torch.empty((m, s.top_k), dtype=torch.int32, device=self.device) if topk else None
+        w = torch.empty((m, s.top_k), dtype=torch.float32, device=self.device) if topk else None
+        self._order()
+        B.dec_run_layer(self.ctx, layer, h_in, m, pos, h_out, idx, w)
+        torch.cuda.current_stream(self.device).wait_stream(self.stream)
+        return (h_out, idx, w) if topk else h_out
+
+    def lm_head(self, h_in: torch.Tensor):
+        """The final norm and LM head on their own: logits into ``self.logits[:m]``; returns the
+        m argmaxes."""
+        self._order()
+        return B.dec_lm_head(self.ctx, h_in, h_in.shape[0], self.logits)
+
     def generate(self, token: int, pos: int, n: int, out: torch.Tensor | None = None) -> torch.Tensor:
         out = out if out is not None else torch.empty(n, dtype=torch.int32, device=self.device)
         self._order()

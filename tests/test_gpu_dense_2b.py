@@ -1,6 +1,10 @@
 """Full-size parity of the 2B-class dense decoder (28 layers, hidden 2560, GQA 20/4, FFN
 6912, vocab 32768, KV prefill 4096) in the launch configuration the bench times: persistent
-megakernel, one CTA per SM, greedy steps chained on the device (GPU)."""
+megakernel, one CTA per SM, greedy steps chained on the device (GPU).
+
+Drift along the chain is checked teacher-forced: at steps 0, 1, 32 and 64 of a device-chained
+greedy run, every one of the 28 layers is recomputed by the oracle from the GPU's own input to
+it, over a cache holding the prefill plus the GPU's own rows of the earlier steps."""
 import numpy as np
 import pytest
 import torch
@@ -12,6 +16,7 @@ from tests.harness import TOL, rel_err, weights, top2_margin
 pytestmark = pytest.mark.gpu
 
 STEPS = 6
+CHECK_STEPS = (0, 1, 32, 64)
 
 
 @pytest.fixture(scope="module")
@@ -68,3 +73,35 @@ def test_modes_agree_at_full_size(setup):
         assert B.dec_last_launch_count(ctx) == 4 * (5 * 28 + 1)
         assert out.cpu().tolist() == ref.cpu().tolist(), mode
         B.dec_free(ctx)
+
+
+def test_teacher_forced_layers_along_chain(setup):
+    s, seed, dec, orc = setup
+    pos0 = s.kv_prefill
+    tok = synth.start_token(seed, s.vocab)
+    done = 0
+    for p in CHECK_STEPS:
+        if p > done:  # the steps in between: greedy, chained on the device
+            out = dec.generate(tok, pos0 + done, p - done)
+            dec.sync()
+            tok = int(out[-1].item())
+        am = dec.step(tok, pos0 + p)
+        hs = dec.hidden_stream()[:, 0].cpu().numpy().astype(np.float64)
+        kc = dec.k_cache[:, :, pos0:pos0 + p].cpu().numpy().view(np.uint16)
+        vc = dec.v_cache[:, :, pos0:pos0 + p].cpu().numpy().view(np.uint16)
+        errs = []
+        for l in range(s.n_layers):
+            orc.K[l][:, pos0:pos0 + p] = kc[l]
+            orc.V[l][:, pos0:pos0 + p] = vc[l]
+            x_in = orc.embed(tok) if l == 0 else hs[2 * l]
+            y = orc.attention_block(l, x_in, pos0 + p)
+            z = orc.ffn_block(l, hs[2 * l + 1], {})
+            errs += [rel_err(hs[2 * l + 1], y), rel_err(hs[2 * l + 2], z)]
+        assert max(errs) <= TOL, (p, int(np.argmax(errs)), max(errs))
+        lg_ref = orc.logits(hs[2 * s.n_layers])
+        lg = dec.logits[0].cpu().numpy()
+        assert rel_err(lg, lg_ref) <= TOL, (p, rel_err(lg, lg_ref))
+        if top2_margin(lg_ref) > 1e-4 * np.max(np.abs(lg_ref)):
+            assert am == int(np.argmax(lg_ref)), (p, am, int(np.argmax(lg_ref)))
+        tok = am
+        done = p + 1
