@@ -116,7 +116,7 @@ int count_ops(const dec_config* c) {
   for (int l = 0; l < c->n_layers; ++l) {
     if (c->n_q) n += 3;
     if (c->ffn) n += 2;
-    if (c->n_experts) n += 3 + (c->n_shared ? 1 : 0);
+    if (c->n_experts) n += 3;
   }
   if (c->vocab) n += 1;
   return n;
@@ -193,7 +193,8 @@ bool compute_layout(const dec_config* c, Layout& L, std::string& why) {
   if (c->n_experts) {
     act = std::max(act, (size_t)M * c->n_experts);
     const size_t per_slot = (size_t)M * c->moe_inter + 2 * (size_t)rows_cta * M;
-    const size_t all = (size_t)(c->n_shared + c->top_k * M) * M * c->moe_inter + 2 * (size_t)rows_cta * M;
+    // every slot's hidden vectors, the residual rows and one set of partial sums per warp
+    const size_t all = (size_t)(c->n_shared + c->top_k * M) * M * c->moe_inter + (1 + kConsumerWarps) * (size_t)rows_cta * M;
     if (all <= std::max(act, (size_t)7168)) {
       act = std::max(act, all);
       L.exp_stage_all = 1;
@@ -344,7 +345,7 @@ struct ListBuilder {
     // the CTA's warps instead of its rows (bf16 / FP8 matrices without expert slots)
     const int cw = o.wtype == W_BF16 ? 8 : (o.wtype == W_FP8 ? 16 : 32);
     const int ni = o.wtype == W_BF16 ? 10 : (o.wtype == W_FP8 ? 5 : 3);
-    const bool experts = o.type == OP_SHARED_GATEUP || o.type == OP_ROUTED_GATEUP || o.type == OP_EXP_DOWN;
+    const bool experts = o.type == OP_ROUTED_GATEUP || o.type == OP_EXP_DOWN;
     if (!experts && o.type != OP_LMHEAD && o.wtype != W_MXFP4 && (o.Kc < o.K || o.K > 32 * ni * cw)) {
       const int kw = ((o.K + kConsumerWarps - 1) / kConsumerWarps + cw - 1) / cw * cw;
       const int bpc = o.wtype == W_BF16 ? 2 : 1;
@@ -459,29 +460,8 @@ struct ListBuilder {
       r.aux_ctr = r.ctr;  // the routing waits for every CTA's logits
       geom(r);
       ops.push_back(r);
-      const int x_ready = r.wait_ctr;  // the shared experts read x' like the router
+      const int x_ready = r.wait_ctr;  // the experts' gate/up reads x' like the router
 
-      if (g.n_shared) {
-        OpDesc sg = blank(OP_SHARED_GATEUP);
-        sg.layer = l;
-        sg.wtype = W_MXFP4;
-        sg.N = 2 * I;
-        sg.K = H;
-        sg.pair = 1;
-        sg.norm = 1;
-        sg.gain = static_cast<const uint16_t*>(w.ffn_norm);
-        sg.w = w.egu_v;
-        sg.ws = w.egu_s;
-        sg.w_mstride = gu_v;
-        sg.ws_mstride = gu_s;
-        sg.slot0 = 0;
-        sg.slot1 = g.n_shared;
-        sg.eh = eh;
-        sg.route = route;
-        sg.wait_ctr = x_ready;
-        geom(sg);
-        ops.push_back(sg);
-      }
       OpDesc rg = blank(OP_ROUTED_GATEUP);
       rg.layer = l;
       rg.wtype = W_MXFP4;
@@ -494,7 +474,7 @@ struct ListBuilder {
       rg.ws = w.egu_s;
       rg.w_mstride = gu_v;
       rg.ws_mstride = gu_s;
-      rg.slot0 = g.n_shared;
+      rg.slot0 = 0;  // every slot: the shared experts first, then the routed ones
       rg.slot1 = -1;
       rg.eh = eh;
       rg.route = route;
@@ -521,6 +501,16 @@ struct ListBuilder {
       dn.x_out = hs_at(2 * l + 2);
       dn.stage_all = L.exp_stage_all;
       geom(dn);
+      if (dn.stage_all && dn.Kc == dn.K) {
+        // slot split: the CTA's rows of each slot in about two chunks, one chunk per warp item
+        const int C = L.n_ctas, units = (H / dn.unit + C - 1) / C;
+        const int nr_max = M == 1 ? 10 : 8;  // the kernel's tile rows for one token / a window
+        int R = (units + 1) / 2 * dn.unit;
+        const size_t row_b = (size_t)I / 2 + I / 32;
+        while (R > dn.unit && (R > nr_max || (size_t)R * row_b + 16 > (size_t)L.slot_bytes)) R -= dn.unit;
+        dn.R = R;
+        dn.csplit = 1;
+      }
       ops.push_back(dn);
       prev = dn.ctr;
       xsrc = X_F32;

@@ -44,8 +44,7 @@ enum OpType : int32_t {
   OP_GATEUP = 3,        // b = RMSNorm(x'); h = silu(W_g b) * (W_u b)   (pair-interleaved rows)
   OP_DOWN = 4,          // x'' = x' + W_d h
   OP_ROUTER = 5,        // b = RMSNorm(x'); r = W_r b (fp32); top-k + softmax (every CTA, locally)
-  OP_SHARED_GATEUP = 6, // h_s = SwiGLU gate/up of the shared experts (MXFP4)
-  OP_ROUTED_GATEUP = 7, // h_e = SwiGLU gate/up of the routed experts (MXFP4)
+  OP_ROUTED_GATEUP = 7, // h_e = SwiGLU gate/up of every slot: shared experts, then routed (MXFP4)
   OP_EXP_DOWN = 8,      // x'' = x' + sum_slots w * W_d,e h_e
   OP_LMHEAD = 9,        // logits = W_lm RMSNorm(x); argmax (block, then last CTA)
 };
@@ -63,6 +62,7 @@ struct OpDesc {
   int32_t slot0, slot1;               // expert slots [slot0, slot1) (slot1 < 0: up to n_slots)
   int32_t x_idx, unit;                // hidden-stream entry of x (X_F32); row granularity of the CTA split
   int32_t stage_all, csplit;          // expert down: all hidden vectors staged; column split across warps
+                                      // (expert down: slot split, chunks of R rows per warp item)
   const void* w;                      // packed values (expert ops: expert 0)
   const void* ws;                     // scales plane (FP8 row scales / MXFP4 E8M0), else null
   int64_t w_mstride, ws_mstride;      // bytes between experts

@@ -156,10 +156,9 @@ __device__ __noinline__ bool wait_counter_slow(const KParams& p, const uint32_t*
 #ifndef DEC_STREAM_EVICT_FIRST
 #define DEC_STREAM_EVICT_FIRST 1  // weights / KV history stream through L2 as evict-first
 #endif
-#ifndef DEC_INFLIGHT_KB
-#define DEC_INFLIGHT_KB 256  // bytes of weight / KV copies one SM may keep in flight, in KiB
+#ifndef DEC_L2_AHEAD
+#define DEC_L2_AHEAD 4  // tiles per warp the producer asks L2 for beyond its ring while the ring waits
 #endif
-constexpr int kInflightBytes = DEC_INFLIGHT_KB * 1024;
 #ifndef DEC_POLL_DATA
 #define DEC_POLL_DATA 1  // 1: no arrival counts: consumers poll the tagged inputs directly
 #endif
@@ -266,11 +265,13 @@ struct Tile {
 struct GemvIter {
   int mode;      // 0: one matrix; 1: expert gate/up (rows run across slots); 2: expert down (slots
                  // outer); 3: column split (every warp covers all of the CTA's rows, warp w columns
-                 // [kw0, kw1))
+                 // [kw0, kw1)); 4: expert down, slot split (the CTA's rows of every slot cut into
+                 // nch chunks of R rows; warp w takes items w, w + 7, ... of slot-major order)
   int N, K, R, Kc;
   int aw, bw, s0, s1;
   int r, kc, sl;
   int kw0, kw1;
+  int nch, item;
   const int* experts;  // expert id per slot (routed ops); null: expert id = mat_base + slot
   int mat_base;
 
@@ -281,19 +282,30 @@ struct GemvIter {
     R = op.R;
     Kc = op.Kc;
     experts = expert_ids;
-    mode = (op.type == OP_SHARED_GATEUP || op.type == OP_ROUTED_GATEUP) ? 1 : (op.type == OP_EXP_DOWN ? 2 : 0);
-    if (op.csplit) mode = 3;
+    if (op.type == OP_ROUTED_GATEUP)
+      mode = 1;
+    else if (op.type == OP_EXP_DOWN)
+      mode = op.csplit ? 4 : 2;
+    else
+      mode = op.csplit ? 3 : 0;
     s0 = 0;
     s1 = 1;
     if (mode == 1) {
       s0 = op.slot0;
-      s1 = op.type == OP_SHARED_GATEUP ? op.slot1 : n_slots;
-    } else if (mode == 2) {
+      s1 = n_slots;
+    } else if (mode == 2 || mode == 4) {
       s1 = n_slots;
     }
     int a, b;
     cta_rows(mode == 1 ? (s1 - s0) * N : N, op.unit, C, cta, a, b);
-    if (mode == 3) {
+    nch = 0;
+    item = w;
+    if (mode == 4) {
+      aw = a;
+      bw = b;
+      nch = b > a ? (b - a + R - 1) / R : 0;
+      kw0 = kw1 = 0;
+    } else if (mode == 3) {
       aw = a;
       bw = b;
       kw0 = min(K, w * Kc);
@@ -308,6 +320,19 @@ struct GemvIter {
   }
 
   __device__ __forceinline__ bool next(Tile& t) {
+    if (mode == 4) {
+      if (item >= (s1 - s0) * nch) return false;
+      const int slot = s0 + item / nch, c = item % nch;
+      t.mat = experts ? experts[slot] : mat_base + slot;
+      t.sl = slot;
+      t.r0 = aw + c * R;
+      t.nr = min(R, bw - t.r0);
+      t.kc = 0;
+      t.kn = K;
+      t.last_k = true;
+      item += kConsumerWarps;
+      return true;
+    }
     if (mode == 3) {
       if (r >= bw || kw0 >= kw1) return false;
       t.mat = 0;
@@ -487,6 +512,34 @@ struct Producer {
     stream(d + bytes, op->vc + off, bytes, fb);
   }
 
+  // Ask L2 for the bytes a tile will bring (cp.async.bulk.prefetch: no completion to wait for).
+  // Sizes are multiples of 16 bytes and starts 16-byte aligned, like the copies themselves; the
+  // MXFP4 scale run is rounded down (its last bytes come with the copy).
+  __device__ __forceinline__ void prefetch_tile(const OpDesc* op, int type, const Tile& t) {
+    if (type == OP_ATTN) {
+      const uint32_t bytes = (uint32_t)t.nr * 256u;
+      const size_t off = ((size_t)t.mat * p.cap + t.r0) * kHeadDim;
+      prefetch_l2(op->kc + off, bytes);
+      prefetch_l2(op->vc + off, bytes);
+      return;
+    }
+    const int wtype = __ldg(&op->wtype), K = __ldg(&op->K);
+    const int rb = row_bytes(wtype, K);
+    const char* base = static_cast<const char*>(op->w) + (size_t)t.mat * __ldg(&op->w_mstride);
+    const int cb = wtype == W_MXFP4 ? t.kn / 2 : t.kn * bytes_per_col(wtype);
+    const int koff = wtype == W_MXFP4 ? t.kc / 2 : t.kc * bytes_per_col(wtype);
+    if (t.kn == K) {
+      prefetch_l2(base + (size_t)t.r0 * rb, (uint32_t)(cb * t.nr));
+    } else {
+      for (int i = 0; i < t.nr; ++i) prefetch_l2(base + (size_t)(t.r0 + i) * rb + koff, (uint32_t)cb);
+    }
+    if (wtype == W_MXFP4 && t.kn == K) {
+      const uint32_t sbytes = (uint32_t)(t.nr * (K / 32)) & ~15u;
+      const char* sb = static_cast<const char*>(op->ws) + (size_t)t.mat * __ldg(&op->ws_mstride);
+      if (sbytes) prefetch_l2(sb + (size_t)t.r0 * (K / 32), sbytes);
+    }
+  }
+
   // Bytes a tile brings into its slot.
   __device__ __forceinline__ uint32_t tile_bytes(const OpDesc* op, int type, const Tile& t) const {
     if (type == OP_ATTN) return (uint32_t)t.nr * 512u;
@@ -513,7 +566,7 @@ struct Producer {
             if (!experts) return false;  // routing not computed yet
             n_slots = s.route->n_slots;
           }
-          c.g.init(*op, p.n_ctas, blockIdx.x, w, n_slots, experts, type == OP_SHARED_GATEUP ? p.E : 0);
+          c.g.init(*op, p.n_ctas, blockIdx.x, w, n_slots, experts, 0);
         }
         c.started = 1;
       }
@@ -552,11 +605,14 @@ struct Producer {
     ++c.n;
   }
 
-  // Lane w streams consumer warp w's tiles. The lanes share one budget of bytes in flight per
-  // SM: a deep queue of weight copies in front of the memory system would make every
-  // latency-critical load of the consumers (activations, counters) wait behind it, while a
-  // budget of about bandwidth x latency keeps HBM just as busy. Each round, one lane whose
-  // warp has a free slot (taken in turn) issues its next tile if the SM is under budget.
+  // Lane w streams consumer warp w's tiles: each round, every lane whose warp has a free slot
+  // issues its next tile (the ring itself bounds the bytes in flight). When no lane can issue
+  // (the consumers are waiting for an op's input, so their rings stay full), the lanes walk on
+  // past their rings and ask L2 for up to DEC_L2_AHEAD more tiles each: HBM keeps streaming
+  // through the hand-off instead of idling, and the ring's later copies of those tiles hit L2
+  // (the Muse Spark Open megakernel article, section "three bills", prefetches the next task's
+  // weights into L2 the same way; measured here, prefetching only while the ring waits beats
+  // prefetching whole ops ahead, which competed with the current op's copies).
   __device__ __forceinline__ void run(int lane) {
     if (lane >= kConsumerWarps) return;
     constexpr unsigned kMask = (1u << kConsumerWarps) - 1u;
@@ -565,10 +621,8 @@ struct Producer {
     c.oi = p.op_begin;
     c.started = 0;
     c.n = 0;
-    uint32_t bytes[kStages];
-#pragma unroll
-    for (int k = 0; k < kStages; ++k) bytes[k] = 0;
-    int rr = 0;
+    LaneCursor pf = c;  // L2-prefetch cursor: at or ahead of the ring's
+    uint32_t pf_n = 0;
     uint64_t t_idle = 0;
     for (;;) {
       Tile t;
@@ -579,41 +633,39 @@ struct Producer {
       const uint32_t st = c.n % (uint32_t)kStages;
       const bool ready =
           have && mbar_test_wait(smem_addr(&s.empty[w * kStages + st]), ((c.n / (uint32_t)kStages) & 1u) ^ 1u);
-      // bytes of this lane's copies not landed yet (only the last kStages can be in flight)
-      uint32_t fl = 0;
-#pragma unroll
-      for (int k = 1; k <= kStages; ++k) {
-        if ((uint32_t)k <= c.n) {
-          const uint32_t q = c.n - k;
-          if (!mbar_test_wait(smem_addr(&s.full[w * kStages + q % kStages]), (q / kStages) & 1u))
-            fl += bytes[q % kStages];
-        }
-      }
-      const uint32_t total = __reduce_add_sync(kMask, fl);
-      // ready lanes in turn from lane rr, each while the SM stays under its budget
-      const uint32_t tb = ready ? tile_bytes(p.ops + c.oi, __ldg(&p.ops[c.oi].type), t) : 0u;
-      const int my_turn = (w - rr + kConsumerWarps) % kConsumerWarps;
-      uint32_t before = 0;
-#pragma unroll
-      for (int k = 0; k < kConsumerWarps; ++k) {
-        const uint32_t bk = __shfl_sync(kMask, tb, k);
-        if ((k - rr + kConsumerWarps) % kConsumerWarps < my_turn) before += bk;
-      }
-      const bool grant = ready && total + before < (uint32_t)kInflightBytes;
+      // every lane whose warp has a free slot issues its next tile (the ring bounds the bytes in flight)
+      const bool grant = ready;
       const unsigned granted = __ballot_sync(kMask, grant);
-      if (grant) {
-        bytes[st] = tb;
-        issue(c, w, t, pa, pg);
-      }
+      if (grant) issue(c, w, t, pa, pg);
       const bool issued = granted != 0u;
-      if (issued) rr = (rr + 1) % kConsumerWarps;
       if (__all_sync(kMask, done)) break;
       if (issued) {
         t_idle = 0;
         continue;
       }
-      // nothing issued: slots full, budget spent or routing pending; back off so the spinning
-      // lanes leave the scheduler's issue slots to the consumers
+      // nothing issued: slots full or routing pending. While the ring waits, each
+      // lane asks L2 for the tiles after its ring, up to DEC_L2_AHEAD of them, so HBM keeps
+      // streaming through a hand-off; the ring's copies of those tiles then hit L2.
+      {
+        if (pf_n < c.n) {
+          pf = c;
+          pf_n = c.n;
+        }
+        Tile tp;
+        AttnIter pa2;
+        GemvIter pg2;
+        bool did = false;
+        if (pf_n < c.n + (uint32_t)DEC_L2_AHEAD && peek(pf, w, tp, pa2, pg2)) {
+          const int ptype = __ldg(&p.ops[pf.oi].type);
+          prefetch_tile(p.ops + pf.oi, ptype, tp);
+          if (ptype == OP_ATTN) pf.a = pa2;
+          else pf.g = pg2;
+          ++pf_n;
+          did = true;
+        }
+        if (__any_sync(kMask, did)) continue;
+      }
+      // back off so the spinning lanes leave the scheduler's issue slots to the consumers
       __nanosleep(64);
       int stop = 0;
       if (w == 0) {
@@ -772,6 +824,8 @@ __device__ __noinline__ bool gemv_tiles_entry(const KParams& p, int oi, const Op
                                               float* accd);
 template <int WT, int MT, int NR, int NI>
 __device__ __noinline__ bool gemv_csplit_entry(const KParams& p, int oi, const OpDesc& op, int M, int a, float* parts);
+template <int MT, int NR, int NI>
+__device__ __noinline__ bool gemv_xsplit_entry(const KParams& p, int oi, const OpDesc& op, int M, int a, float* parts);
 template <int MT>
 __device__ __noinline__ bool gemv_slot_entry(const KParams& p, int oi, const OpDesc& op, int sl, int M, int a,
                                              float* accd);
@@ -1081,48 +1135,51 @@ struct Consumer {
         M * E, [&](int i) { return op.act + i; }, [&](int i, const float (&v)[1]) { r[i] = v[0]; }, oi, 10);
     if (!consumer_all(ok)) return false;
     RouteBlock* rb = s.route;
-    for (int m = 0; m < M; ++m) {
-      for (int kk = 0; kk < k; ++kk) {
-        float bv = -INFINITY;
-        int bi = 0x7FFFFFFF;
-        for (int e = tid; e < E; e += kConsumerThreads) {
-          const float v = r[m * E + e];
-          if (v > bv || (v == bv && e < bi)) {
+    // Top-k per token, one warp per token (warp m < M takes token m): lane l owns logits
+    // l, l + 32, ... and keeps its best one not yet taken; each of the k rounds reduces the
+    // lanes' bests over the warp (larger logit first, lower index on ties), and the lane that
+    // owned the winner takes it out and rescans its own logits. No CTA barrier inside.
+    if (warp < M) {
+      float* rm = r + warp * E;
+      auto lane_best = [&](float& bv, int& bi) {
+        bv = -INFINITY;
+        bi = 0x7FFFFFFF;
+        for (int e = lane; e < E; e += 32) {
+          const float v = rm[e];
+          if (v > bv) {  // ascending e: an equal later logit never replaces the lower index
             bv = v;
             bi = e;
           }
         }
+      };
+      float bv;
+      int bi;
+      lane_best(bv, bi);
+      for (int kk = 0; kk < k; ++kk) {
+        float v = bv;
+        int i = bi;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
-          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-          const int oj = __shfl_xor_sync(0xffffffffu, bi, o);
-          if (ov > bv || (ov == bv && oj < bi)) {
-            bv = ov;
-            bi = oj;
+          const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+          const int oi = __shfl_xor_sync(0xffffffffu, i, o);
+          if (ov > v || (ov == v && oi < i)) {
+            v = ov;
+            i = oi;
           }
         }
+        if (i >= E) i = kk;  // no ordered logit left (NaN inputs): an in-range id, never a wild one
         if (lane == 0) {
-          s.red[warp] = bv;
-          s.resw[warp] = __int_as_float(bi);
+          rb->topk[warp][kk] = i;
+          rb->topk_w[warp][kk] = v;  // the logit, replaced by its weight below
         }
-        consumer_sync();
-        if (tid == 0) {
-          float v = s.red[0];
-          int i = __float_as_int(s.resw[0]);
-          for (int w = 1; w < kConsumerWarps; ++w) {
-            const int wi = __float_as_int(s.resw[w]);
-            if (s.red[w] > v || (s.red[w] == v && wi < i)) {
-              v = s.red[w];
-              i = wi;
-            }
-          }
-          rb->topk[m][kk] = i;
-          rb->topk_w[m][kk] = v;  // the logit, replaced by its weight below
-          r[m * E + i] = -INFINITY;
+        if ((i & 31) == lane) {  // the owner takes the winner out and finds its next best
+          rm[i] = -INFINITY;
+          lane_best(bv, bi);
         }
-        consumer_sync();
+        __syncwarp();
       }
     }
+    consumer_sync();
     if (tid == 0) {
       for (int m = 0; m < M; ++m) {
         const float mx = rb->topk_w[m][0];
@@ -1180,8 +1237,7 @@ struct Consumer {
     GemvIter it;
     const bool routed = op.type == OP_ROUTED_GATEUP || op.type == OP_EXP_DOWN;
     const int n_slots = routed ? s.route->n_slots : 0;
-    it.init(op, p.n_ctas, blockIdx.x, warp, n_slots, routed ? s.route->expert : nullptr,
-            op.type == OP_SHARED_GATEUP ? p.E : 0);
+    it.init(op, p.n_ctas, blockIdx.x, warp, n_slots, routed ? s.route->expert : nullptr, 0);
     Acc<NR, MT> A;
     acc_zero(A);
     float best_v = -INFINITY;
@@ -1221,7 +1277,6 @@ struct Consumer {
           if (mine) put_x(op, m, t.r0 + i, xres[(t.r0 + i - a) * M + m] + v);
           break;
         case OP_GATEUP:
-        case OP_SHARED_GATEUP:
         case OP_ROUTED_GATEUP: {
           // rows come in (gate, up) pairs: lanes (2jj)*MT + m and (2jj+1)*MT + m hold them
           const int jj = lane / MT;
@@ -1315,11 +1370,51 @@ struct Consumer {
     for (int t = tid; t < rows * M; t += kConsumerThreads) {
       const int r = t / M, m = t % M;
       const float v = rowsum(r, m);
-      if (op.type == OP_OPROJ || op.type == OP_DOWN)
+      if (op.type == OP_OPROJ || op.type == OP_DOWN || op.type == OP_EXP_DOWN)
         put_x(op, m, a + r, xres[t] + v);
       else
         st_tagged(op.out + (size_t)m * op.N + a + r, v, tag);
     }
+  }
+
+  // Expert down, slot split (all hidden vectors staged): warp w takes chunks of R rows of the
+  // slots in the GemvIter order, and adds each chunk's row sums, weighted by the token's routing
+  // weight of that slot, to its own partial sums parts[w][row][m]; csplit_epilogue adds the
+  // warps' partials in warp order and the residual. NI > 0: one token, the slot's activations
+  // reloaded into registers whenever the slot changes.
+  template <int MT, int NR, int NI>
+  __device__ __forceinline__ bool gemv_xsplit_t(int oi, const OpDesc& op, int M, int a, float* parts) {
+    GemvIter it;
+    it.init(op, p.n_ctas, blockIdx.x, warp, s.route->n_slots, s.route->expert, 0);
+    const int rows = it.bw - it.aw;
+    float* pw = parts + warp * rows * M;
+    Acc<NR, MT> A;
+    static_assert(NI == 0 || MT == 1, "register activations serve one token");
+    ActRegs<W_MXFP4, (NI > 0 ? NI : 1)> AR;
+    int cur = -1;
+    const int i = lane / MT, m = lane % MT;
+    Tile t;
+    while (it.next(t)) {
+      uint8_t* slot;
+      uint32_t eb;
+      if (!next_slot(oi, slot, eb)) return false;
+      const float* act = s.act + (size_t)t.sl * M * op.K;
+      if constexpr (NI > 0) {
+        if (t.sl != cur) {
+          act_regs_load(AR, act, op.K, 0, op.K, lane);
+          cur = t.sl;
+        }
+      }
+      acc_zero(A);
+      if constexpr (NI > 0)
+        warp_gemv_reg<W_MXFP4, NR, NI>(slot, t.nr, t.kn, AR, A, lane);
+      else
+        warp_gemv<W_MXFP4, MT, NR>(slot, t.nr, t.kn, 0, act, op.K, M, A, lane);
+      release(eb);
+      const float v = warp_rowsums<NR, MT>(A, t.nr, lane);
+      if (lane < t.nr * MT && m < M) pw[(t.r0 + i - a) * M + m] += s.route->w[m][t.sl] * v;
+    }
+    return true;
   }
 
   // Instantiations: tile rows NR (bf16 2/4/8, FP8 4/8, MXFP4 8; the host's R fits) and, for
@@ -1453,7 +1548,8 @@ struct Consumer {
         break;
       case OP_EXP_DOWN:
         ok &= load_residual(op, g.xres, g.a, g.b, M, oi);
-        for (int t = tid; t < (g.b - g.a) * M; t += kConsumerThreads) g.accd[t] = 0.f;
+        // partial sums: one set per warp in the slot split, one for the CTA otherwise
+        for (int t = tid; t < (op.csplit ? kConsumerWarps : 1) * (g.b - g.a) * M; t += kConsumerThreads) g.accd[t] = 0.f;
         if (op.stage_all)
           for (int sl = 0; sl < s.route->n_slots; ++sl)
             ok &= copy_act(s.act + (size_t)sl * M * op.K, op.eh + (size_t)sl * p.Mmax * op.K, M, op.K, op.K, cw, oi);
@@ -1483,6 +1579,13 @@ struct Consumer {
                               : gemv_slot_entry<4>(p, oi, op, sl, M, g.a, g.accd);
         if (!consumer_all(r)) return false;
       }
+    } else if (op.type == OP_EXP_DOWN && op.csplit) {
+      bool r;
+      if (M == 1)  // activations from shared memory: a register copy of the slot's would spill
+        r = gemv_xsplit_entry<1, 10, 0>(p, oi, op, M, g.a, g.accd);
+      else
+        r = gemv_xsplit_entry<4, 8, 0>(p, oi, op, M, g.a, g.accd);
+      if (!consumer_all(r)) return false;
     } else {
       const bool r = M == 1 ? gemv_dispatch<1>(oi, op, M, g.xres, g.a, g.accd)
                             : gemv_dispatch<4>(oi, op, M, g.xres, g.a, g.accd);
@@ -1497,7 +1600,7 @@ struct Consumer {
   __device__ __forceinline__ bool gemv_epilogue(int oi, const OpDesc& op, int M) {
     const GemvGeo g = gemv_geo(op, M);
     if (op.csplit) csplit_epilogue(op, M, g.a, g.b, g.xres, g.accd);
-    if (op.type == OP_EXP_DOWN) {
+    if (op.type == OP_EXP_DOWN && !op.csplit) {
       for (int t = tid; t < (g.b - g.a) * M; t += kConsumerThreads) {
         const int i = t / M, m = t % M;
         put_x(op, m, g.a + i, g.xres[t] + g.accd[t]);
@@ -1542,7 +1645,7 @@ struct Consumer {
             i = ci;
           }
         }
-        p.am_out[tid] = i;
+        p.am_out[tid] = i < p.V ? i : 0;  // no ordered logit (NaN inputs): a valid token, never a wild one
       }
     }
   }
@@ -1839,6 +1942,14 @@ template <int WT, int MT, int NR, int NI>
 __device__ __noinline__ bool gemv_csplit_entry(const KParams& p, int oi, const OpDesc& op, int M, int a, float* parts) {
   Consumer c(p);
   const bool ok = c.gemv_csplit_t<WT, MT, NR, NI>(oi, op, M, a, parts);
+  c.save_tiles();
+  return ok;
+}
+
+template <int MT, int NR, int NI>
+__device__ __noinline__ bool gemv_xsplit_entry(const KParams& p, int oi, const OpDesc& op, int M, int a, float* parts) {
+  Consumer c(p);
+  const bool ok = c.gemv_xsplit_t<MT, NR, NI>(oi, op, M, a, parts);
   c.save_tiles();
   return ok;
 }

@@ -37,7 +37,7 @@ def op_types(shape) -> list[str]:
         if shape.ffn:
             out += ["gateup", "down"]
         if shape.n_experts:
-            out += ["router"] + (["shared_gateup"] if shape.n_shared else []) + ["routed_gateup", "exp_down"]
+            out += ["router", "routed_gateup", "exp_down"]
     if shape.vocab:
         out.append("lm_head")
     return out
