@@ -388,6 +388,7 @@ def main():
     ap.add_argument("--workload", default="dense_2b", choices=sorted(WORKLOADS))
     ap.add_argument("--verify", type=int, default=1, choices=[1, 2, 3, 4],
                     help="> 1: time verify windows of this many tokens")
+    ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"], help="KV cache format (fp8: e4m3, scales 1.0)")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling captures only: fewer decoder layers (the line is then not the workload's)")
     args = ap.parse_args()
@@ -412,11 +413,12 @@ def main():
     layers = head = kv = None
     if args.workload == "dense_2b":
         s, layers, head, kv = build_workload(args.seed, args.layers)
+        s = s.with_(kv_dtype=args.kv)
         cap = s.kv_prefill + chain + 8
         dec = Decoder(s, layers, head, kv=kv, capacity=cap, mode=args.mode, device=dev)
     else:
         from tests.device_inputs import device_decoder
-        s = workload_shape(args.workload, args.layers)
+        s = workload_shape(args.workload, args.layers).with_(kv_dtype=args.kv)
         chain = s.steps
         dec = device_decoder(s, args.seed, s.kv_prefill + chain + 8, dev, mode=args.mode)
     tok0 = synth.start_token(args.seed, s.vocab)
@@ -441,7 +443,8 @@ def main():
     launch_s = secs / launches
     peak, peak_kind = peaks()
     achieved = bytes_step * (1 if args.mode == "persistent" else 1) / (secs / args.steps) / 1e9
-    traffic = ncu_traffic(args.workload, kernel_sources()) if args.mode == "persistent" and not args.layers else None
+    traffic_key = args.workload + ("_kv8" if args.kv == "fp8" else "")
+    traffic = ncu_traffic(traffic_key, kernel_sources()) if args.mode == "persistent" and not args.layers else None
 
     # end to end through the C ABI with host buffers: token in, argmax out, every step
     K2 = min(args.steps, chain)
@@ -476,7 +479,8 @@ def main():
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * secs_max / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": WORKLOADS[args.workload].format(L=s.n_layers),
+            "config": {"workload": WORKLOADS[args.workload].format(L=s.n_layers) +
+                                   (", FP8 e4m3 KV cache (scales 1.0)" if args.kv == "fp8" else ""),
                        "weights": ("bf16 ~N(0,0.02) seeded, accumulate fp32" if args.workload == "dense_2b" else
                                    "bf16 attention / router / embedding, MXFP4 experts and FP8 head quantised from "
                                    "seeded bf16 ~N(0,0.02), drawn and packed on the device; accumulate fp32"),

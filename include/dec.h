@@ -53,6 +53,8 @@ typedef enum {
   DEC_FP8_E4M3_ROWSCALE = 1, /* e4m3fn codes, 1 B per weight, plus one fp32 scale per row */
   DEC_MXFP4 = 2,           /* e2m1 codes (2 per byte, even element low nibble) plus one
                               E8M0 scale byte per 32 consecutive weights of a row */
+  DEC_FP8_E4M3 = 3,        /* KV cache: e4m3fn codes, 1 B per element, value = s * e4m3(q)
+                              with one fp32 scale s per (layer, keys or values, kv head) */
 } dec_dtype;
 
 typedef enum {
@@ -83,6 +85,7 @@ typedef struct {
   dec_mode mode;
   uint64_t spin_timeout_ns; /* limit of every device wait (0: 2 s) */
   int num_ctas;      /* persistent CTAs (0: one per SM) */
+  dec_dtype kv_dtype; /* KV cache: DEC_BF16 (0) or DEC_FP8_E4M3 */
 } dec_config;
 
 typedef struct dec_ctx dec_ctx;
@@ -127,14 +130,21 @@ dec_status dec_init(const dec_config* cfg, void* cuda_stream, void* workspace_de
    dec_free). Tags and shapes are checked against the config; may be called repeatedly. */
 dec_status dec_load_weights(dec_ctx* ctx, const dec_tensor* tensors, int n);
 
-/* Register the KV cache: k_dev and v_dev are bf16 [n_layers][n_kv][kv_capacity][head_dim],
-   caller-owned device memory, each 256-byte aligned (DEC_ERR_INVALID_ARG otherwise).
-   Positions below the step's pos must hold the cached (already rotated) keys and values; a
-   step writes its own rows at pos.. before attending over them (the Muse Spark Open
-   megakernel article, section "three bills": the layer's KV write comes before the attention
-   that reads it; the Kimi-K3 8xB300 benchmark page reads the long-context cache this way).
-   DEC_ERR_STATE for a config without attention. */
+/* Register the KV cache: k_dev and v_dev are [n_layers][n_kv][kv_capacity][head_dim], bf16, or
+   e4m3fn codes (1 byte) when kv_dtype = DEC_FP8_E4M3; caller-owned device memory, each 256-byte
+   aligned (DEC_ERR_INVALID_ARG otherwise). Positions below the step's pos must hold the cached
+   (already rotated) keys and values; a step writes its own rows at pos.. before attending over
+   them (the Muse Spark Open megakernel article, section "three bills": the layer's KV write
+   comes before the attention that reads it; the Kimi-K3 8xB300 benchmark page reads the
+   long-context cache this way). DEC_ERR_STATE for a config without attention. */
 dec_status dec_set_kv_cache(dec_ctx* ctx, void* k_dev, void* v_dev);
+
+/* Scales of an FP8 KV cache (kv_dtype = DEC_FP8_E4M3; the Kimi-K3 8xB300 benchmark, section on
+   its log warnings: fp8_e4m3 caches whose scaling factor defaults to 1.0): scales_dev is fp32
+   [n_layers][2][n_kv] on the device (index 0 keys, 1 values), caller-owned; NULL (the state
+   after dec_init) makes every scale 1.0. A new key or value x is stored as
+   e4m3fn(round-to-nearest-even of x / s in fp32, saturated to +-448). */
+dec_status dec_set_kv_scales(dec_ctx* ctx, const float* scales_dev);
 
 /* One decode step of `token` at position `pos` (embedding configs), or of the given hidden
    vector hidden_dev (bf16 [H], device, 16-byte aligned; non-embedding configs, token ignored):
@@ -296,6 +306,13 @@ dec_status dec_pack_device(dec_dtype dtype, const uint16_t* bf16_dev, int rows, 
 dec_status dec_pack_pair_device(dec_dtype dtype, const uint16_t* a_dev, const uint16_t* b_dev,
                                 int rows, int cols, void* out_values, void* out_scales,
                                 void* stream);
+
+/* FP8 KV-cache entries from bf16 values: out[i] = e4m3fn(RNE of v[i] / scale in fp32, saturated
+   to +-448), the rule the kernel applies to new rows; n elements, host or device memory. The
+   device form is queued on `stream` and returns without waiting. */
+dec_status dec_pack_kv_fp8(const uint16_t* bf16_host, size_t n, float scale, uint8_t* out_host);
+dec_status dec_pack_kv_fp8_device(const uint16_t* bf16_dev, size_t n, float scale, uint8_t* out_dev,
+                                  void* stream);
 
 #ifdef __cplusplus
 }

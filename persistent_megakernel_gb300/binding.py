@@ -25,6 +25,7 @@ DEC_ERR_CAPACITY = 7
 DEC_BF16 = 0
 DEC_FP8_E4M3_ROWSCALE = 1
 DEC_MXFP4 = 2
+DEC_FP8_E4M3 = 3
 
 DEC_MODE_PERSISTENT = 0
 DEC_MODE_PER_OP = 1
@@ -36,8 +37,9 @@ DEC_MODE_PER_OP_GRAPH = 2
 # every symbol include/dec.h declares
 EXPORTS = ("dec_workspace_bytes", "dec_init", "dec_load_weights", "dec_set_kv_cache", "dec_step", "dec_generate",
            "dec_verify", "dec_debug_buffers", "dec_reset", "dec_sync", "dec_last_launch_count", "dec_last_error",
-           "dec_free", "dec_packed_bytes", "dec_pack", "dec_pack_pair", "dec_pack_device", "dec_pack_pair_device", "dec_trace_buffer", "dec_lm_head_noalloc", "dec_debug_drop_op",
-           "dec_run_layer", "dec_lm_head")
+           "dec_free", "dec_packed_bytes", "dec_pack", "dec_pack_pair", "dec_pack_device", "dec_pack_pair_device",
+           "dec_set_kv_scales", "dec_pack_kv_fp8", "dec_pack_kv_fp8_device", "dec_trace_buffer", "dec_lm_head_noalloc",
+           "dec_debug_drop_op", "dec_run_layer", "dec_lm_head")
 
 
 class DecConfig(ctypes.Structure):
@@ -46,7 +48,7 @@ class DecConfig(ctypes.Structure):
         "vocab", "kv_capacity", "max_verify", "embedding", "final_norm")] + [
         ("rms_eps", ctypes.c_float), ("rope_base", ctypes.c_float),
         ("lm_head_dtype", ctypes.c_int), ("expert_dtype", ctypes.c_int), ("mode", ctypes.c_int),
-        ("spin_timeout_ns", ctypes.c_uint64), ("num_ctas", ctypes.c_int)]
+        ("spin_timeout_ns", ctypes.c_uint64), ("num_ctas", ctypes.c_int), ("kv_dtype", ctypes.c_int)]
 
 
 class DecTensor(ctypes.Structure):
@@ -75,6 +77,9 @@ def lib():
             "dec_init": (I, [ctypes.POINTER(DecConfig), P, P, ctypes.POINTER(P)]),
             "dec_load_weights": (I, [P, ctypes.POINTER(DecTensor), I]),
             "dec_set_kv_cache": (I, [P, P, P]),
+            "dec_set_kv_scales": (I, [P, P]),
+            "dec_pack_kv_fp8": (I, [P, SZ, ctypes.c_float, P]),
+            "dec_pack_kv_fp8_device": (I, [P, SZ, ctypes.c_float, P, P]),
             "dec_step": (I, [P, ctypes.c_int32, P, ctypes.c_int32, P, P]),
             "dec_generate": (I, [P, ctypes.c_int32, ctypes.c_int32, I, P]),
             "dec_run_layer": (I, [P, I, P, I, ctypes.c_int32, P, P, P]),
@@ -236,3 +241,15 @@ def dec_pack_pair_device(dtype: int, a_dev, b_dev, rows: int, cols: int, out_val
                          stream=None) -> None:
     check(lib().dec_pack_pair_device(dtype, _p(a_dev), _p(b_dev), rows, cols, _p(out_values_dev), _p(out_scales_dev),
                                      _p(stream)))
+
+
+def dec_set_kv_scales(ctx: int, scales_dev) -> None:
+    check(lib().dec_set_kv_scales(ctx, _p(scales_dev)))
+
+
+def dec_pack_kv_fp8(bf16, n: int, scale: float, out) -> None:
+    check(lib().dec_pack_kv_fp8(_p(bf16), n, scale, _p(out)))
+
+
+def dec_pack_kv_fp8_device(bf16_dev, n: int, scale: float, out_dev, stream=None) -> None:
+    check(lib().dec_pack_kv_fp8_device(_p(bf16_dev), n, scale, _p(out_dev), _p(stream)))

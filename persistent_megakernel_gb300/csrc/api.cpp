@@ -24,6 +24,8 @@ extern "C" cudaError_t dec_launch_megakernel(const KParams* kp, int cooperative,
 extern "C" int dec_megakernel_common_bytes(void);
 extern "C" cudaError_t dec_launch_pack(int dtype, const uint16_t* a, const uint16_t* b, int rows, int cols,
                                        void* vals, void* scales, cudaStream_t stream);
+extern "C" cudaError_t dec_launch_pack_kv_fp8(const uint16_t* v, size_t n, float s, uint8_t* out,
+                                              cudaStream_t stream);
 
 namespace {
 
@@ -99,6 +101,7 @@ bool validate(const dec_config* c, std::string& why) {
   if (c->embedding && c->vocab <= 0) return bad("embedding needs a vocabulary");
   if (c->mode < DEC_MODE_PERSISTENT || c->mode > DEC_MODE_PER_OP_GRAPH) return bad("bad mode");
   if (c->num_ctas < 0) return bad("num_ctas must be >= 0");
+  if (c->kv_dtype != DEC_BF16 && c->kv_dtype != DEC_FP8_E4M3) return bad("kv_dtype must be DEC_BF16 or DEC_FP8_E4M3");
   if (!std::isfinite(c->rms_eps) || c->rms_eps < 0) return bad("rms_eps must be >= 0");
   return true;
 }
@@ -261,8 +264,9 @@ struct dec_ctx {
   const void* final_norm = nullptr;
   const void* lm_v = nullptr;
   const void* lm_s = nullptr;
-  uint16_t* kc = nullptr;
-  uint16_t* vc = nullptr;
+  uint8_t* kc = nullptr;   // bf16 or e4m3 rows (kv_row_bytes)
+  uint8_t* vc = nullptr;
+  const float* kv_scales = nullptr;  // FP8 cache: [n_layers][2][n_kv] (null: all 1)
   bool ops_dirty = true;
   std::vector<OpDesc> ops;
   KParams kp;
@@ -390,8 +394,10 @@ struct ListBuilder {
       a.act = q.out;
       a.out = wsp<uint64_t>(c, L.attn_out) + (size_t)l * M * g.n_q * kHeadDim;
       a.aux_ctr = L.n_ops + l * g.n_kv;  // per-kv-head counters of the splits' partials
-      a.kc = c->kc + (size_t)l * g.n_kv * g.kv_capacity * kHeadDim;
-      a.vc = c->vc + (size_t)l * g.n_kv * g.kv_capacity * kHeadDim;
+      const size_t kv_layer = (size_t)l * g.n_kv * g.kv_capacity * kv_row_bytes(g.kv_dtype == DEC_FP8_E4M3);
+      a.kc = c->kc + kv_layer;
+      a.vc = c->vc + kv_layer;
+      a.kv_scale = c->kv_scales ? c->kv_scales + (size_t)l * 2 * g.n_kv : nullptr;
       ops.push_back(a);
       prev = a.ctr;
 
@@ -570,6 +576,7 @@ void fill_params(dec_ctx* c, KParams& k, size_t ops_off, int n_ops) {
   k.timeout_ns = g.spin_timeout_ns ? g.spin_timeout_ns : 2000000000ull;
   k.slot_bytes = L.slot_bytes;
   k.act_bytes = L.act_bytes;
+  k.kv_fp8 = g.kv_dtype == DEC_FP8_E4M3 ? 1 : 0;
   k.state = wsp<StepState>(c, L.state);
   k.status = wsp<Status>(c, L.status);
   k.tickets = wsp<uint32_t>(c, L.tickets);
@@ -884,8 +891,18 @@ dec_status dec_set_kv_cache(dec_ctx* c, void* k_dev, void* v_dev) {
   if (!c->cfg.n_q) return fail(DEC_ERR_STATE, "config has no attention");
   if (!k_dev || !v_dev || reinterpret_cast<uintptr_t>(k_dev) % 256 || reinterpret_cast<uintptr_t>(v_dev) % 256)
     return fail(DEC_ERR_INVALID_ARG, "KV cache pointers must be non-null and 256-byte aligned");
-  c->kc = static_cast<uint16_t*>(k_dev);
-  c->vc = static_cast<uint16_t*>(v_dev);
+  c->kc = static_cast<uint8_t*>(k_dev);
+  c->vc = static_cast<uint8_t*>(v_dev);
+  c->ops_dirty = true;
+  return DEC_OK;
+}
+
+dec_status dec_set_kv_scales(dec_ctx* c, const float* scales_dev) {
+  if (!c) return fail(DEC_ERR_INVALID_ARG, "null context");
+  if (!c->cfg.n_q || c->cfg.kv_dtype != DEC_FP8_E4M3) return fail(DEC_ERR_STATE, "config has no FP8 KV cache");
+  if (scales_dev && reinterpret_cast<uintptr_t>(scales_dev) % 4)
+    return fail(DEC_ERR_INVALID_ARG, "KV scales must be 4-byte aligned");
+  c->kv_scales = scales_dev;
   c->ops_dirty = true;
   return DEC_OK;
 }
@@ -1161,6 +1178,13 @@ dec_status dec_pack_pair_device(dec_dtype dtype, const uint16_t* a_dev, const ui
                                 void* out_values, void* out_scales, void* stream) {
   if (!b_dev) return fail(DEC_ERR_INVALID_ARG, "null device pointer");
   return pack_device(dtype, a_dev, b_dev, rows, cols, out_values, out_scales, stream);
+}
+
+dec_status dec_pack_kv_fp8_device(const uint16_t* v, size_t n, float scale, uint8_t* out, void* stream) {
+  if (n && (!v || !out)) return fail(DEC_ERR_INVALID_ARG, "null device pointer");
+  if (!(scale > 0.f) || !std::isfinite(scale)) return fail(DEC_ERR_INVALID_ARG, "KV scale must be positive and finite");
+  CUDA_TRY(dec_launch_pack_kv_fp8(v, n, scale, out, static_cast<cudaStream_t>(stream)));
+  return DEC_OK;
 }
 
 void dec_free(dec_ctx* c) {

@@ -74,8 +74,9 @@ struct OpDesc {
   uint64_t* out;                      // output, tagged: qkv [Mmax][qkv], h [Mmax][F], router logits,
                                       // attention out [Mmax][n_q 128]
   float* logits;                      // LM head: fp32 logits [Mmax][V] (plain, for the caller)
-  uint16_t* kc;                       // this layer's key cache  bf16 [n_kv][cap][128]
-  uint16_t* vc;                       // this layer's value cache bf16 [n_kv][cap][128]
+  uint8_t* kc;                        // this layer's key cache   [n_kv][cap][128] bf16 or e4m3
+  uint8_t* vc;                        // this layer's value cache [n_kv][cap][128] bf16 or e4m3
+  const float* kv_scale;              // FP8 cache: this layer's scales [2][n_kv] (null: all 1)
   int32_t* route;                     // this layer's RouteBlock
   uint64_t* eh;                       // this layer's expert hidden, tagged [slots][Mmax][I]
   uint16_t* y_bf16;                   // residual ops: also store the output rounded to bf16 here,
@@ -119,6 +120,7 @@ struct KParams {
   float eps, rope_base;
   uint64_t timeout_ns;
   int32_t slot_bytes, act_bytes;      // bytes of one warp's ring slot; shared-memory scratch
+  int32_t kv_fp8, pad1;               // 1: the KV cache holds e4m3 codes (128 B per row), else bf16
   StepState* state;
   Status* status;
   uint32_t* tickets;
@@ -149,6 +151,14 @@ constexpr int kTileStamps = 6;
 #define DEC_HD
 #endif
 
+// Bytes of one cached key (or value) row, and the KV rows one ring slot takes (keys then values;
+// at most 32: the softmax keeps one row per lane).
+DEC_HD inline int kv_row_bytes(int kv_fp8) { return kv_fp8 ? 128 : 256; }
+DEC_HD inline int attn_rows_per_slot(int slot_bytes, int kv_fp8) {
+  const int r = slot_bytes / (2 * kv_row_bytes(kv_fp8));
+  return r < 32 ? r : 32;
+}
+
 // Attention scratch inside a CTA's activation area, in floats from its (256-byte aligned) start;
 // the kernel carves it and the host sizes the area with the same function. P: KV rows per
 // ring slot; ns: splits per kv head.
@@ -165,7 +175,7 @@ DEC_HD inline AttnLayout attn_layout(int M, int G, int P, int ns) {
   l.sc = l.q + MG * 128;                                        // per-warp scores / merge slices
   l.mg = up4(l.sc + (kConsumerWarps * G * P > prods ? kConsumerWarps * G * P : prods));
   l.kvn = l.mg + kConsumerWarps * G * kPart;                    // per-warp split states
-  l.cw = l.kvn + kMmax * 128;                                   // own keys / values (bf16 [2][M][128])
+  l.cw = l.kvn + kMmax * 128;                                   // own keys / values ([2][M][128] bf16 or e4m3)
   l.ml = up4(l.cw + MG * ns);                                   // merge weights
   l.raw = up4(l.ml + 2 * MG * ns);                              // splits' (max, sum)
   l.end = l.raw + M * (G + 2) * 128;                            // polled q / k / v rows

@@ -504,8 +504,9 @@ struct Producer {
   }
 
   __device__ __forceinline__ void copy_attn(const OpDesc* op, const Tile& t, uint8_t* dst, uint32_t fb) {
-    const uint32_t bytes = (uint32_t)t.nr * 256u;
-    const size_t off = ((size_t)t.mat * p.cap + t.r0) * kHeadDim;
+    const int rb = kv_row_bytes(p.kv_fp8);
+    const uint32_t bytes = (uint32_t)(t.nr * rb);
+    const size_t off = ((size_t)t.mat * p.cap + t.r0) * rb;  // bytes
     mbar_expect_tx(fb, 2u * bytes);
     const uint32_t d = smem_addr(dst);
     stream(d, op->kc + off, bytes, fb);
@@ -517,8 +518,9 @@ struct Producer {
   // MXFP4 scale run is rounded down (its last bytes come with the copy).
   __device__ __forceinline__ void prefetch_tile(const OpDesc* op, int type, const Tile& t) {
     if (type == OP_ATTN) {
-      const uint32_t bytes = (uint32_t)t.nr * 256u;
-      const size_t off = ((size_t)t.mat * p.cap + t.r0) * kHeadDim;
+      const int rb = kv_row_bytes(p.kv_fp8);
+      const uint32_t bytes = (uint32_t)(t.nr * rb);
+      const size_t off = ((size_t)t.mat * p.cap + t.r0) * rb;  // bytes
       prefetch_l2(op->kc + off, bytes);
       prefetch_l2(op->vc + off, bytes);
       return;
@@ -542,7 +544,7 @@ struct Producer {
 
   // Bytes a tile brings into its slot.
   __device__ __forceinline__ uint32_t tile_bytes(const OpDesc* op, int type, const Tile& t) const {
-    if (type == OP_ATTN) return (uint32_t)t.nr * 512u;
+    if (type == OP_ATTN) return (uint32_t)(t.nr * 2 * kv_row_bytes(p.kv_fp8));
     const int wtype = __ldg(&op->wtype);
     if (wtype == W_MXFP4) return (uint32_t)(t.nr * (t.kn / 2) + t.nr * (t.kn / 32));
     return (uint32_t)(t.nr * t.kn * bytes_per_col(wtype));
@@ -557,7 +559,7 @@ struct Producer {
       const int type = __ldg(&op->type);
       if (!c.started) {
         if (type == OP_ATTN) {
-          c.a.init(p, blockIdx.x, w, pos, M, s.slot_bytes / 512);
+          c.a.init(p, blockIdx.x, w, pos, M, attn_rows_per_slot(s.slot_bytes, p.kv_fp8));
         } else {
           const int* experts = nullptr;
           int n_slots = 0;
@@ -733,25 +735,42 @@ struct AttnState {
   float o[G_][4];  // this lane's dims 4*lane .. +3
 };
 
-// One tile of n rows (keys at kr, values at vr; 256 B per row) for the G_ heads of token m.
+// e4m3fn code (bits 0-7 of x) -> float, exactly: the code's 7 low bits go to fp32 bits 20-26
+// and its sign to bit 31, which is the value times 2^-120 (subnormal codes become fp32
+// subnormals); the multiply by 2^120 restores it.
+__device__ __forceinline__ float e4m3_to_float_bits(uint32_t x) {
+  return __uint_as_float(((x & 0x7Fu) << 20) | ((x & 0x80u) << 24)) * 0x1p120f;
+}
+
+// One tile of n rows (keys at kr, values at vr; 256 B per bf16 row, 128 B per e4m3 row) for the
+// G_ heads of token m. e4m3 rows hold the codes: the caller folds the keys' scale into q and
+// applies the values' scale to the outputs.
 // vis_base < 0: all rows visible; else row j is this call's row vis_base + j, visible iff <= m.
-template <int G_>
+template <int G_, bool KV8>
 __device__ __forceinline__ void attn_warp_tile(AttnState<G_>& A, const float (&q)[G_][16], const uint8_t* kr,
                                                const uint8_t* vr, int n, int vis_base, int m, float* sc, int P,
                                                int lane) {
+  constexpr int RB = KV8 ? 128 : 256;
   const int grp = lane >> 3, sub = lane & 7;
   // scores: eight lanes per row, 16 dims each, four rows per step
   for (int j0 = 0; j0 < n; j0 += 4) {
     const int j = j0 + grp;
     float kf[16];
     if (j < n) {
-      const uint4 k0 = *reinterpret_cast<const uint4*>(kr + (size_t)j * 256 + sub * 32);
-      const uint4 k1 = *reinterpret_cast<const uint4*>(kr + (size_t)j * 256 + sub * 32 + 16);
-      const uint32_t kw[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+      if constexpr (KV8) {
+        const uint4 k0 = *reinterpret_cast<const uint4*>(kr + (size_t)j * RB + sub * 16);
+        const uint32_t kw[4] = {k0.x, k0.y, k0.z, k0.w};
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        kf[2 * e] = bf16_lo(kw[e]);
-        kf[2 * e + 1] = bf16_hi(kw[e]);
+        for (int e = 0; e < 16; ++e) kf[e] = e4m3_to_float_bits(kw[e >> 2] >> (8 * (e & 3)));
+      } else {
+        const uint4 k0 = *reinterpret_cast<const uint4*>(kr + (size_t)j * RB + sub * 32);
+        const uint4 k1 = *reinterpret_cast<const uint4*>(kr + (size_t)j * RB + sub * 32 + 16);
+        const uint32_t kw[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          kf[2 * e] = bf16_lo(kw[e]);
+          kf[2 * e + 1] = bf16_hi(kw[e]);
+        }
       }
     } else {
 #pragma unroll
@@ -799,9 +818,16 @@ __device__ __forceinline__ void attn_warp_tile(AttnState<G_>& A, const float (&q
 #pragma unroll
     for (int e = 0; e < 4; ++e) A.o[h][e] *= scale[h];
   for (int j = 0; j < n; ++j) {
-    const uint2 v = *reinterpret_cast<const uint2*>(vr + (size_t)j * 256 + lane * 8);
-    const float2 v01 = make_float2(bf16_lo(v.x), bf16_hi(v.x));
-    const float2 v23 = make_float2(bf16_lo(v.y), bf16_hi(v.y));
+    float2 v01, v23;
+    if constexpr (KV8) {
+      const uint32_t v = *reinterpret_cast<const uint32_t*>(vr + (size_t)j * RB + lane * 4);
+      v01 = make_float2(e4m3_to_float_bits(v), e4m3_to_float_bits(v >> 8));
+      v23 = make_float2(e4m3_to_float_bits(v >> 16), e4m3_to_float_bits(v >> 24));
+    } else {
+      const uint2 v = *reinterpret_cast<const uint2*>(vr + (size_t)j * RB + lane * 8);
+      v01 = make_float2(bf16_lo(v.x), bf16_hi(v.x));
+      v23 = make_float2(bf16_lo(v.y), bf16_hi(v.y));
+    }
 #pragma unroll
     for (int h = 0; h < G_; ++h) {
       const float pj = sc[h * P + j];
@@ -1655,7 +1681,8 @@ struct Consumer {
   __device__ __forceinline__ bool attn_op(int oi, const OpDesc& op, int pos, int M) {
     if (op.wait_ctr >= 0 && !wait_counter(op.wait_ctr, op.wait_n, oi, 4)) return false;
     if (tid == 0) TRACE(p, oi, 1, gtimer());
-    const int P = s.slot_bytes / 512;
+    const int P = attn_rows_per_slot(s.slot_bytes, p.kv_fp8);
+    const int rb = kv_row_bytes(p.kv_fp8);
     const int G = G_, MG = M * G, ns = p.ns_max;
     const AttnScratch a = attn_scratch(p, s, M, P);
     const float qscale = 1.4426950408889634f / sqrtf(128.f);  // log2(e) / sqrt(d)
@@ -1699,25 +1726,46 @@ struct Consumer {
         a.q[mh * 128 + i] = (x1 * cs.x - x2 * cs.y) * qscale;
         a.q[mh * 128 + i + 64] = (x1 * cs.y + x2 * cs.x) * qscale;
       }
+      // FP8 cache: this layer's key / value scales of the group's kv head (1 without scales)
+      const float sk = p.kv_fp8 && op.kv_scale ? op.kv_scale[head] : 1.f;
+      const float sv = p.kv_fp8 && op.kv_scale ? op.kv_scale[p.n_kv + head] : 1.f;
       for (int idx = tid; idx < nn * 64; idx += kConsumerThreads) {
         const int r = idx >> 6, i = idx & 63;
         const int m = nb - pos + r;
         const float* kr = a.raw + m * GR * 4 + G * 128;
         const float* vr = kr + 128;
         const float2 cs = s.rope[m * 64 + i];
-        const uint16_t b1 = __bfloat16_as_ushort(__float2bfloat16_rn(kr[i] * cs.x - kr[i + 64] * cs.y));
-        const uint16_t b2 = __bfloat16_as_ushort(__float2bfloat16_rn(kr[i] * cs.y + kr[i + 64] * cs.x));
-        const uint16_t c1 = __bfloat16_as_ushort(__float2bfloat16_rn(vr[i]));
-        const uint16_t c2 = __bfloat16_as_ushort(__float2bfloat16_rn(vr[i + 64]));
-        a.kvn[r * 128 + i] = b1;
-        a.kvn[r * 128 + i + 64] = b2;
-        a.kvn[(nn + r) * 128 + i] = c1;
-        a.kvn[(nn + r) * 128 + i + 64] = c2;
-        const size_t off = ((size_t)head * p.cap + pos + m) * kHeadDim;  // append to the KV history
-        op.kc[off + i] = b1;
-        op.kc[off + i + 64] = b2;
-        op.vc[off + i] = c1;
-        op.vc[off + i + 64] = c2;
+        const float k1 = kr[i] * cs.x - kr[i + 64] * cs.y, k2 = kr[i] * cs.y + kr[i + 64] * cs.x;
+        const size_t row = (size_t)head * p.cap + pos + m;  // append to the KV history
+        if (p.kv_fp8) {
+          // e4m3fn of x / s: the fp32 quotient rounded to nearest even, saturated to +-448
+          const uint8_t b1 = e4m3_rn_satfinite(__fdiv_rn(k1, sk)), b2 = e4m3_rn_satfinite(__fdiv_rn(k2, sk));
+          const uint8_t c1 = e4m3_rn_satfinite(__fdiv_rn(vr[i], sv)), c2 = e4m3_rn_satfinite(__fdiv_rn(vr[i + 64], sv));
+          uint8_t* kvn8 = reinterpret_cast<uint8_t*>(a.kvn);
+          kvn8[r * 128 + i] = b1;
+          kvn8[r * 128 + i + 64] = b2;
+          kvn8[(nn + r) * 128 + i] = c1;
+          kvn8[(nn + r) * 128 + i + 64] = c2;
+          op.kc[row * 128 + i] = b1;
+          op.kc[row * 128 + i + 64] = b2;
+          op.vc[row * 128 + i] = c1;
+          op.vc[row * 128 + i + 64] = c2;
+        } else {
+          const uint16_t b1 = __bfloat16_as_ushort(__float2bfloat16_rn(k1));
+          const uint16_t b2 = __bfloat16_as_ushort(__float2bfloat16_rn(k2));
+          const uint16_t c1 = __bfloat16_as_ushort(__float2bfloat16_rn(vr[i]));
+          const uint16_t c2 = __bfloat16_as_ushort(__float2bfloat16_rn(vr[i + 64]));
+          a.kvn[r * 128 + i] = b1;
+          a.kvn[r * 128 + i + 64] = b2;
+          a.kvn[(nn + r) * 128 + i] = c1;
+          a.kvn[(nn + r) * 128 + i + 64] = c2;
+          uint16_t* kc16 = reinterpret_cast<uint16_t*>(op.kc);
+          uint16_t* vc16 = reinterpret_cast<uint16_t*>(op.vc);
+          kc16[row * 128 + i] = b1;
+          kc16[row * 128 + i + 64] = b2;
+          vc16[row * 128 + i] = c1;
+          vc16[row * 128 + i + 64] = c2;
+        }
       }
       consumer_sync();
       if (tid == 0 && it.j == (int)blockIdx.x) {
@@ -1737,7 +1785,7 @@ struct Consumer {
 #pragma unroll
       for (int h = 0; h < G_; ++h)
 #pragma unroll
-        for (int e = 0; e < 16; ++e) q[h][e] = a.q[(m_tok * G + h) * 128 + sub * 16 + e];
+        for (int e = 0; e < 16; ++e) q[h][e] = a.q[(m_tok * G + h) * 128 + sub * 16 + e] * sk;
       Tile t;
       while (it.next_in_split(t)) {
         uint8_t* slot;
@@ -1746,13 +1794,19 @@ struct Consumer {
           ok = false;
           break;
         }
-        attn_warp_tile<G_>(A, q, slot, slot + t.nr * 256, t.nr, -1, m_tok, sc, P, lane);
+        if (p.kv_fp8)
+          attn_warp_tile<G_, true>(A, q, slot, slot + t.nr * rb, t.nr, -1, m_tok, sc, P, lane);
+        else
+          attn_warp_tile<G_, false>(A, q, slot, slot + t.nr * rb, t.nr, -1, m_tok, sc, P, lane);
         release(eb);
       }
       // this call's own rows: the first warp of each token group attends to them (causally)
       if (ok && gi == 0 && nn > 0) {
         const uint8_t* kn = reinterpret_cast<const uint8_t*>(a.kvn);
-        attn_warp_tile<G_>(A, q, kn, kn + nn * 256, nn, nb - pos, m_tok, sc, P, lane);
+        if (p.kv_fp8)
+          attn_warp_tile<G_, true>(A, q, kn, kn + nn * rb, nn, nb - pos, m_tok, sc, P, lane);
+        else
+          attn_warp_tile<G_, false>(A, q, kn, kn + nn * rb, nn, nb - pos, m_tok, sc, P, lane);
       }
       // per-warp state -> shared memory; merge the warps of each token into the split partial
       float* mg = a.mg + warp * G * kPart;
@@ -1762,8 +1816,9 @@ struct Consumer {
           mg[h * kPart] = A.mrun[h];
           mg[h * kPart + 1] = A.lrun[h];
         }
+        // FP8 cache: the value codes were summed unscaled; sv is 1 for bf16
         *reinterpret_cast<float4*>(mg + h * kPart + 4 + lane * 4) =
-            make_float4(A.o[h][0], A.o[h][1], A.o[h][2], A.o[h][3]);
+            make_float4(A.o[h][0] * sv, A.o[h][1] * sv, A.o[h][2] * sv, A.o[h][3] * sv);
       }
       if (!consumer_all(ok)) return false;
       if (tid == 0) TRACE(p, oi, 3, gtimer());

@@ -78,8 +78,23 @@ __global__ void __launch_bounds__(kPackThreads) pack_rows_kernel(int dtype, cons
   }
 }
 
+// FP8 KV-cache entries: out[i] = e4m3fn(v[i] / s), the host packer's encoder.
+__global__ void __launch_bounds__(kPackThreads) pack_kv_fp8_kernel(const uint16_t* __restrict__ v, size_t n, float s,
+                                                                   uint8_t* __restrict__ out) {
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) out[i] = decq::fp8_code(v[i], s);
+}
+
 }  // namespace
 }  // namespace decimpl
+
+extern "C" cudaError_t dec_launch_pack_kv_fp8(const uint16_t* v, size_t n, float s, uint8_t* out, cudaStream_t stream) {
+  if (n == 0) return cudaSuccess;
+  size_t blocks = (n + decimpl::kPackThreads - 1) / decimpl::kPackThreads;
+  if (blocks > 8192) blocks = 8192;
+  decimpl::pack_kv_fp8_kernel<<<(unsigned)blocks, decimpl::kPackThreads, 0, stream>>>(v, n, s, out);
+  return cudaGetLastError();
+}
 
 // Queue the packing kernel (arguments already validated by the caller).
 extern "C" cudaError_t dec_launch_pack(int dtype, const uint16_t* a, const uint16_t* b, int rows, int cols,

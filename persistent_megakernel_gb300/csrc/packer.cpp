@@ -5,6 +5,7 @@
 // halving its read). MXFP4: OCP Microscaling v1.0 FP4 (e2m1) elements with one E8M0 scale per
 // 32 weights of a row (the MXFP4 experts of the same article, "optimisation 1"). The encoders
 // (quant.h) are the ones the device packer (pack.cu) runs, so both give the same bytes.
+#include <cmath>
 #include <cstdint>
 #include <cstring>
 
@@ -84,6 +85,14 @@ dec_status dec_pack_pair(dec_dtype dtype, const uint16_t* a, const uint16_t* b, 
     pack_row(dtype, a, r, cols, out_values, out_scales, 2 * r);
     pack_row(dtype, b, r, cols, out_values, out_scales, 2 * r + 1);
   }
+  return DEC_OK;
+}
+
+dec_status dec_pack_kv_fp8(const uint16_t* v, size_t n, float scale, uint8_t* out) {
+  if (n && (!v || !out)) return DEC_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return DEC_ERR_INVALID_ARG;
+#pragma omp parallel for schedule(static)
+  for (long long i = 0; i < (long long)n; ++i) out[i] = decq::fp8_code(v[i], scale);
   return DEC_OK;
 }
 

@@ -207,6 +207,14 @@ __device__ __forceinline__ float2 e2m1x2_to_float2(uint32_t byte) {
   return r;
 }
 
+// fp32 -> e4m3fn code: round to nearest even, saturated to +-448 (cvt.rn.satfinite; the second
+// source converts into the low byte).
+__device__ __forceinline__ uint8_t e4m3_rn_satfinite(float x) {
+  uint16_t h;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(h) : "f"(0.f), "f"(x));
+  return (uint8_t)(h & 0xFFu);
+}
+
 // E8M0 scale code -> 2^(e-127) as float (e = 0 gives the subnormal 2^-127).
 __device__ __forceinline__ float e8m0_to_float(uint32_t e) {
   return e ? __uint_as_float(e << 23) : __uint_as_float(0x00400000u);

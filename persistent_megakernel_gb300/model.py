@@ -42,6 +42,7 @@ def make_config(shape, capacity: int, max_verify: int = 1, mode: str = "persiste
     c.mode = _MODE[mode]
     c.spin_timeout_ns = timeout_ns
     c.num_ctas = num_ctas
+    c.kv_dtype = B.DEC_FP8_E4M3 if getattr(shape, "kv_dtype", "bf16") == "fp8" else B.DEC_BF16
     return c
 
 
@@ -85,6 +86,15 @@ def pack_device(dtype: int, w: torch.Tensor, pair_with: torch.Tensor | None = No
     return vals, scales
 
 
+def pack_kv_host(x: np.ndarray, head_scales: np.ndarray) -> np.ndarray:
+    """e4m3 codes of a bf16 cache block [n_kv, n, d] (numpy uint16), head g under head_scales[g]."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    out = np.empty(x.shape, np.uint8)
+    for g in range(x.shape[0]):
+        B.dec_pack_kv_fp8(x[g], x[g].size, float(head_scales[g]), out[g])
+    return out
+
+
 class Decoder:
     """One model instance on one GPU: workspace, packed weights, KV cache, context.
 
@@ -96,14 +106,16 @@ class Decoder:
     experts    : callable (layer, expert) -> (gate, up, down) bf16 for MoE layers; experts
                  shape.n_experts .. + n_shared - 1 are the shared ones
     kv         : list of (K, V) bf16 prefills [n_kv, n, d] per layer, or None (the caller may
-                 fill ``k_cache`` / ``v_cache`` itself before the first step)
+                 fill ``k_cache`` / ``v_cache`` itself before the first step); an FP8 cache
+                 (shape.kv_dtype == "fp8") stores them as e4m3 codes
+    kv_scales  : FP8 cache scales [n_layers, 2 (keys, values), n_kv] (None: all 1.0)
     packed_experts : instead of ``experts``, callable layer -> (gate/up values, gate/up scales,
                  down values, down scales), the MXFP4 planes of all the layer's experts already
                  packed (host arrays or device tensors)
     """
 
     def __init__(self, shape, layers, head, experts=None, kv=None, capacity=None, max_verify=1, mode="persistent",
-                 num_ctas=0, timeout_ns=0, device="cuda:0", packed_experts=None):
+                 num_ctas=0, timeout_ns=0, device="cuda:0", packed_experts=None, kv_scales=None):
         self.shape = shape
         self.device = torch.device(device)
         # a stream of its own: CUDA-graph capture cannot use the legacy default stream
@@ -165,16 +177,26 @@ class Decoder:
         B.dec_load_weights(self.ctx, tensors)
         self._tensors = tensors
 
+        self.kv_fp8 = getattr(s, "kv_dtype", "bf16") == "fp8"
+        self.kv_scales = None
         if s.attn:
-            self.k_cache = torch.zeros((s.n_layers, s.n_kv, self.capacity, s.head_dim), dtype=torch.int16,
-                                       device=self.device)
+            dt = torch.uint8 if self.kv_fp8 else torch.int16
+            self.k_cache = torch.zeros((s.n_layers, s.n_kv, self.capacity, s.head_dim), dtype=dt, device=self.device)
             self.v_cache = torch.zeros_like(self.k_cache)
+            sc = (np.ones((s.n_layers, 2, s.n_kv), np.float32) if kv_scales is None
+                  else np.ascontiguousarray(kv_scales, np.float32))
             if kv is not None:
                 for l, (k, v) in enumerate(kv):
                     n = k.shape[1]
+                    if self.kv_fp8:
+                        # the prefilled bf16 history is stored as e4m3 codes under each head's scale
+                        k, v = pack_kv_host(k, sc[l, 0]), pack_kv_host(v, sc[l, 1])
                     self.k_cache[l, :, :n] = _dev(k, self.device)
                     self.v_cache[l, :, :n] = _dev(v, self.device)
             B.dec_set_kv_cache(self.ctx, self.k_cache, self.v_cache)
+            if self.kv_fp8:
+                self.kv_scales = torch.from_numpy(sc).to(self.device)
+                B.dec_set_kv_scales(self.ctx, self.kv_scales)
         torch.cuda.synchronize(self.device)
         self.logits = torch.empty((max_verify, max(s.vocab, 1)), dtype=torch.float32, device=self.device)
 
@@ -190,6 +212,8 @@ class Decoder:
         B.dec_load_weights(ctx, self._tensors)
         if self.shape.attn:
             B.dec_set_kv_cache(ctx, self.k_cache, self.v_cache)
+            if self.kv_scales is not None:
+                B.dec_set_kv_scales(ctx, self.kv_scales)
         return ctx, ws_all
 
     def _pack_experts(self, experts, l):

@@ -79,16 +79,25 @@ def packed_experts(s, seed: int, layer: int, device="cuda:0"):
     return gu_v, gu_s, dn_v, dn_s
 
 
-def fill_kv_prefill(s, seed: int, k_cache: torch.Tensor, v_cache: torch.Tensor) -> None:
+def fill_kv_prefill(s, seed: int, k_cache: torch.Tensor, v_cache: torch.Tensor, kv_scales=None) -> None:
     """Write ``synth.model.kv_prefill`` of every layer into the library's caches
-    [n_layers, n_kv, capacity, head_dim] (rows [0, kv_prefill) of each head)."""
+    [n_layers, n_kv, capacity, head_dim] (rows [0, kv_prefill) of each head). An FP8 cache
+    (uint8) receives the e4m3 codes of the bf16 draws under kv_scales [n_layers, 2, n_kv]."""
+    from persistent_megakernel_gb300 import binding as B
     n, d = s.kv_prefill, s.head_dim
     st = _stream(k_cache.device)
+    fp8 = k_cache.dtype == torch.uint8
+    tmp = torch.empty((n, d), dtype=torch.int16, device=k_cache.device) if fp8 else None
     for l in range(s.n_layers):
         for g in range(s.n_kv):
-            for cache, kind in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+            for kv, (cache, kind) in enumerate(((k_cache, "k_cache"), (v_cache, "v_cache"))):
                 dst = cache[l, g, :n]
-                synth.normal_bf16_dev(dst, seed, tensor_id(kind, l), 0.0, 1.0, g * n * d, st)
+                if not fp8:
+                    synth.normal_bf16_dev(dst, seed, tensor_id(kind, l), 0.0, 1.0, g * n * d, st)
+                    continue
+                synth.normal_bf16_dev(tmp, seed, tensor_id(kind, l), 0.0, 1.0, g * n * d, st)
+                scale = 1.0 if kv_scales is None else float(kv_scales[l][kv][g])
+                B.dec_pack_kv_fp8_device(tmp, n * d, scale, dst, st)
 
 
 def device_decoder(s, seed: int, capacity: int, device="cuda:0", **kw):
@@ -109,6 +118,6 @@ def device_decoder(s, seed: int, capacity: int, device="cuda:0", **kw):
 
     dec = Decoder(s, layers, head, kv=None, capacity=capacity, device=device, packed_experts=experts, **kw)
     if s.attn:
-        fill_kv_prefill(s, seed, dec.k_cache, dec.v_cache)
+        fill_kv_prefill(s, seed, dec.k_cache, dec.v_cache, kw.get("kv_scales"))
     torch.cuda.synchronize(device)
     return dec

@@ -26,7 +26,7 @@ def B():
 def _declared():
     text = open(os.path.join(ROOT, "include", "dec.h")).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(dec_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(dec_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_exports_every_declared_symbol(B):
@@ -183,6 +183,26 @@ def test_mxfp4_packer_every_bf16_value(B, bmax):
     codes, e = F.quantize_mxfp4(w)
     assert np.array_equal(e.reshape(-1), sc)
     assert np.array_equal(codes.reshape(-1), out)
+
+
+@pytest.mark.parametrize("scale", [1.0, 0.3, 3.3, 2.0 ** -5])
+def test_kv_fp8_packer_equals_oracle_quantiser(B, scale):
+    vals = _finite_bf16_upto(0x7F7F)                     # every finite bf16 value
+    out = np.empty(vals.size, np.uint8)
+    B.dec_pack_kv_fp8(vals, vals.size, scale, out)
+    want = F.quantize_kv_fp8(F.bf16_to_f64(vals), scale)
+    assert np.array_equal(out, want)
+
+
+def test_kv_fp8_entry_points_reject_bad_arguments(B):
+    L = B.lib()
+    assert L.dec_set_kv_scales(None, None) == B.DEC_ERR_INVALID_ARG
+    v = np.zeros(4, np.uint16)
+    o = np.zeros(4, np.uint8)
+    assert L.dec_pack_kv_fp8(v.ctypes.data, 4, ctypes.c_float(0.0), o.ctypes.data) == B.DEC_ERR_INVALID_ARG
+    assert L.dec_pack_kv_fp8(None, 4, ctypes.c_float(1.0), o.ctypes.data) == B.DEC_ERR_INVALID_ARG
+    assert L.dec_pack_kv_fp8_device(None, 4, ctypes.c_float(1.0), 0x10000, None) == B.DEC_ERR_INVALID_ARG
+    assert B.dec_workspace_bytes(_cfg(B, kv_dtype=7)) == 0
 
 
 def test_device_packer_rejects_bad_arguments(B):
