@@ -553,6 +553,7 @@ void build_ops(dec_ctx* c) {
   k.am_idx = wsp<int32_t>(c, L.am_idx);
   k.am_out = wsp<int32_t>(c, L.am_out);
   k.step_ticket = ticket++;
+  k.n_steps = 1;
   k.hs = hs;
 #ifdef DEC_TRACE
   k.trace = wsp<uint64_t>(c, L.trace);
@@ -576,10 +577,12 @@ dec_status prepare(dec_ctx* c) {
   return DEC_OK;
 }
 
-dec_status launch_step(dec_ctx* c) {
+// One step, or (persistent mode, n_steps > 1) n chained greedy steps in one launch.
+dec_status launch_step(dec_ctx* c, int n_steps = 1) {
   KParams k = c->kp;
   const dec_mode mode = c->cfg.mode;
   if (mode == DEC_MODE_PERSISTENT) {
+    k.n_steps = n_steps;
     CUDA_TRY(dec_launch_megakernel(&k, 1, c->stream));
     c->last_launches = 1;
     return DEC_OK;
@@ -864,6 +867,10 @@ dec_status dec_generate(dec_ctx* c, int32_t token, int32_t pos, int n, int32_t* 
     return fail(DEC_ERR_CAPACITY, "positions %d..%d exceed kv_capacity %d", pos, pos + n - 1, c->cfg.kv_capacity);
   st = write_state(c, pos, 1, &token, nullptr, 1, tokens_dev);
   if (st != DEC_OK) return st;
+  if (c->cfg.mode == DEC_MODE_PERSISTENT) {
+    // the whole chain in one launch: the kernel feeds each step's argmax to the next step
+    return launch_step(c, n);
+  }
   int launches = 0;
   for (int i = 0; i < n; ++i) {
     st = launch_step(c);
@@ -1018,6 +1025,7 @@ dec_status dec_lm_head_noalloc(int hidden, int vocab, dec_dtype dtype, int m, fl
   k.am_idx = reinterpret_cast<int32_t*>(scratch + off_idx);
   k.am_out = argmax_dev;
   k.step_ticket = 1;
+  k.n_steps = 1;
 
   // the scratch keeps the previous call's contents: everything the kernel counts from starts at zero
   cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
