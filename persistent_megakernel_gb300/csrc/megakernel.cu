@@ -522,6 +522,13 @@ struct Producer {
       const int type = __ldg(&op->type);
       if (!c.started) {
         if (type == OP_ATTN) {
+          // a later step's attention reads cache rows the earlier steps appended: wait until
+          // this CTA has taken the state of that step (its consumers passed the step end)
+          if (c.step > 0) {
+            const uint32_t e = *reinterpret_cast<volatile const uint32_t*>(&g_st.epoch);
+            if ((int32_t)(e - (epoch0 + (uint32_t)c.step)) < 0) return false;
+            __threadfence_block();
+          }
           c.a.init(p, blockIdx.x, w, pos + c.step, M, s.slot_bytes / 512);
         } else {
           const int* experts = nullptr;
@@ -1914,7 +1921,12 @@ __device__ __noinline__ bool next_step_state(const KParams& p) {
       __threadfence();
       const uint32_t* src = reinterpret_cast<const uint32_t*>(p.state);
       uint32_t* dst = reinterpret_cast<uint32_t*>(&g_st);
-      for (int i = 0; i < (int)(sizeof(StepState) / 4); ++i) dst[i] = __ldcg(src + i);
+      // every other field first; the epoch last, which the producer lanes poll
+      constexpr int kEpochWord = (int)(offsetof(StepState, epoch) / 4);
+      for (int i = 0; i < (int)(sizeof(StepState) / 4); ++i)
+        if (i != kEpochWord) dst[i] = __ldcg(src + i);
+      __threadfence_block();
+      *reinterpret_cast<volatile uint32_t*>(&g_st.epoch) = __ldcg(src + kEpochWord);
     }
   }
   return consumer_all(ok);
