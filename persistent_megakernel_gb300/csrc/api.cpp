@@ -586,6 +586,7 @@ void fill_params(dec_ctx* c, KParams& k, size_t ops_off, int n_ops) {
   k.am_idx = wsp<int32_t>(c, L.am_idx);
   k.am_out = wsp<int32_t>(c, L.am_out);
   k.step_ticket = kStepTicket;
+  k.n_steps = 1;
   k.hs = wsp<uint64_t>(c, L.hs);
 #ifdef DEC_TRACE
   k.trace = wsp<uint64_t>(c, L.trace);
@@ -621,11 +622,13 @@ dec_status prepare(dec_ctx* c) {
 
 // Launch an op list in the context's mode. The CUDA graph of the per-op-graph mode holds the
 // whole step's list; other lists (a layer or the LM head on its own) run as plain per-op launches
-// in that mode.
-dec_status launch_list(dec_ctx* c, const KParams& k, bool whole_step) {
+// in that mode. Persistent mode with n_steps > 1: n chained greedy steps in one launch.
+dec_status launch_list(dec_ctx* c, const KParams& k0, bool whole_step, int n_steps = 1) {
+  KParams k = k0;
   dec_mode mode = c->cfg.mode;
   if (mode == DEC_MODE_PER_OP_GRAPH && !whole_step) mode = DEC_MODE_PER_OP;
   if (mode == DEC_MODE_PERSISTENT) {
+    k.n_steps = n_steps;
     CUDA_TRY(dec_launch_megakernel(&k, 1, c->stream));
     c->last_launches = 1;
     return DEC_OK;
@@ -985,6 +988,10 @@ dec_status dec_generate(dec_ctx* c, int32_t token, int32_t pos, int n, int32_t* 
     return fail(DEC_ERR_CAPACITY, "positions %d..%d exceed kv_capacity %d", pos, pos + n - 1, c->cfg.kv_capacity);
   st = write_state(c, pos, 1, &token, nullptr, 1, tokens_dev);
   if (st != DEC_OK) return st;
+  if (c->cfg.mode == DEC_MODE_PERSISTENT) {
+    // the whole chain in one launch: the kernel feeds each step's argmax to the next step
+    return launch_list(c, c->kp, true, n);
+  }
   int launches = 0;
   for (int i = 0; i < n; ++i) {
     st = launch_list(c, c->kp, true);
@@ -1139,6 +1146,7 @@ dec_status dec_lm_head_noalloc(int hidden, int vocab, dec_dtype dtype, int m, fl
   k.am_idx = reinterpret_cast<int32_t*>(scratch + off_idx);
   k.am_out = argmax_dev;
   k.step_ticket = 1;
+  k.n_steps = 1;
 
   // the scratch keeps the previous call's contents: everything the kernel counts from starts at zero
   cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);

@@ -130,6 +130,7 @@ struct KParams {
   int32_t* am_idx;
   int32_t* am_out;                    // argmax [Mmax]
   int32_t step_ticket;                // ticket index of the step-end rendezvous
+  int32_t n_steps, pad2;              // greedy steps this launch runs (> 1: chained in the kernel)
   uint64_t* hs;                       // hidden stream, tagged [2L + 1][Mmax][H]
   uint64_t* trace;                    // DEC_TRACE builds: [n_ctas][n_ops][kTraceFields] %globaltimer stamps
 };

@@ -49,7 +49,7 @@ constexpr int kOffFull = 0, kOffEmpty = 256, kOffOp = 512, kOffRed = 1024, kOffR
               kOffFlags = 7168, kOffRoute = 7232, kOffNTiles = 8192;
 constexpr int kFlagTicket = 1;  // flags[kFlagTicket]: verdict of the last ticket
 constexpr int kFlagLate = 2;    // flags[kFlagLate]: input words re-polled in this op (DEC_TRACE)
-constexpr int kFlagRoute = 8;   // flags[kFlagRoute]: layer + 1 whose routing sits in `route`
+constexpr int kFlagRoute = 8;   // flags[kFlagRoute]: route_tag of the routing that sits in `route`
 static_assert(kConsumerWarps * kStages * 8 <= kOffEmpty - kOffFull, "full barriers");
 static_assert(sizeof(OpDesc) <= kOffRed - kOffOp, "OpDesc copy");
 static_assert(kOffRoute + sizeof(RouteBlock) <= kOffNTiles, "routing block");
@@ -447,8 +447,18 @@ struct AttnIter {
 // for that op's input. The lanes advance together (SIMT), each issuing when its warp has a
 // free slot; a lane stalls only at a routed-expert op until this CTA's consumers have computed
 // the layer's routing.
+// Greedy steps one launch runs (at least one).
+__device__ __forceinline__ int steps_of(const KParams& p) { return p.n_steps > 1 ? p.n_steps : 1; }
+
+// Tag of one MoE layer's routing within one step (epoch: the step's count of completed steps):
+// steps that run in one launch route the same layers again.
+__device__ __forceinline__ int route_tag(uint32_t epoch, int layer, int L) {
+  return (int)((epoch * (uint32_t)(L + 1) + (uint32_t)layer + 1u) & 0x7FFFFFFFu);
+}
+
 struct LaneCursor {
   int oi, started;
+  int step;    // step of the launch the cursor is in (pos + step, epoch0 + step)
   uint32_t n;  // tiles issued to this lane's warp
   GemvIter g;
   AttnIter a;
@@ -457,8 +467,9 @@ struct LaneCursor {
 struct Producer {
   const KParams& p;
   Smem& s;
-  int pos, M;
+  int pos, M;       // of the launch's first step; step k decodes at pos + k
   uint64_t policy;  // L2 policy of the streamed bytes
+  uint32_t epoch0;  // completed steps when the launch began
 
   __device__ __forceinline__ void stream(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
 #if DEC_STREAM_EVICT_FIRST
@@ -469,8 +480,8 @@ struct Producer {
   }
 
   // Expert ids of the current MoE layer's routing, once the consumers have published it.
-  __device__ __forceinline__ const int* routing(const OpDesc* op) {
-    if (s.flags[kFlagRoute] != __ldg(&op->layer) + 1) return nullptr;
+  __device__ __forceinline__ const int* routing(const OpDesc* op, int step) {
+    if (s.flags[kFlagRoute] != route_tag(epoch0 + (uint32_t)step, __ldg(&op->layer), p.L)) return nullptr;
     __threadfence_block();
     return s.route->expert;
   }
@@ -509,6 +520,9 @@ struct Producer {
     const size_t off = ((size_t)t.mat * p.cap + t.r0) * rb;  // bytes
     mbar_expect_tx(fb, 2u * bytes);
     const uint32_t d = smem_addr(dst);
+    // a chained launch reads rows that its own earlier steps appended with plain stores; the
+    // step-end rendezvous orders them before this lane's slot hand-back, this fence before the copy
+    if (p.n_steps > 1) fence_proxy_async_global();
     stream(d, op->kc + off, bytes, fb);
     stream(d + bytes, op->vc + off, bytes, fb);
   }
@@ -554,17 +568,30 @@ struct Producer {
   // Returns false if the lane has no tile to offer right now (all ops done, or a routed op whose
   // routing is not computed yet).
   __device__ __forceinline__ bool peek(LaneCursor& c, int w, Tile& t, AttnIter& pa, GemvIter& pg) {
-    while (c.oi < p.op_end) {
+    for (;;) {
+      if (c.oi >= p.op_end) {
+        if (c.step + 1 >= steps_of(p)) return false;
+        ++c.step;  // the launch's next step: the same ops at the next position
+        c.oi = p.op_begin;
+        c.started = 0;
+      }
       const OpDesc* op = p.ops + c.oi;
       const int type = __ldg(&op->type);
       if (!c.started) {
         if (type == OP_ATTN) {
-          c.a.init(p, blockIdx.x, w, pos, M, attn_rows_per_slot(s.slot_bytes, p.kv_fp8));
+          // a later step's attention reads cache rows the earlier steps appended: wait until
+          // this CTA has taken the state of that step (its consumers passed the step end)
+          if (c.step > 0) {
+            const uint32_t e = *reinterpret_cast<volatile const uint32_t*>(&g_st.epoch);
+            if ((int32_t)(e - (epoch0 + (uint32_t)c.step)) < 0) return false;
+            __threadfence_block();
+          }
+          c.a.init(p, blockIdx.x, w, pos + c.step, M, attn_rows_per_slot(s.slot_bytes, p.kv_fp8));
         } else {
           const int* experts = nullptr;
           int n_slots = 0;
           if (type == OP_ROUTED_GATEUP || type == OP_EXP_DOWN) {
-            experts = routing(op);
+            experts = routing(op, c.step);
             if (!experts) return false;  // routing not computed yet
             n_slots = s.route->n_slots;
           }
@@ -578,7 +605,6 @@ struct Producer {
       ++c.oi;
       c.started = 0;
     }
-    return false;
   }
 
   __device__ __forceinline__ void issue(LaneCursor& c, int w, const Tile& t, const AttnIter& pa, const GemvIter& pg) {
@@ -622,6 +648,7 @@ struct Producer {
     LaneCursor c;
     c.oi = p.op_begin;
     c.started = 0;
+    c.step = 0;
     c.n = 0;
     LaneCursor pf = c;  // L2-prefetch cursor: at or ahead of the ring's
     uint32_t pf_n = 0;
@@ -631,7 +658,7 @@ struct Producer {
       AttnIter pa;
       GemvIter pg;
       const bool have = peek(c, w, t, pa, pg);
-      const bool done = c.oi >= p.op_end;
+      const bool done = c.oi >= p.op_end && c.step + 1 >= steps_of(p);
       const uint32_t st = c.n % (uint32_t)kStages;
       const bool ready =
           have && mbar_test_wait(smem_addr(&s.empty[w * kStages + st]), ((c.n / (uint32_t)kStages) & 1u) ^ 1u);
@@ -1153,7 +1180,7 @@ struct Consumer {
   // and the union of the window's experts (shared experts first). The producer lanes read it
   // from shared memory once flags[kFlagRoute] names the layer. Uses the start of s.act.
   __device__ __forceinline__ bool ensure_routing(const OpDesc& op, int M, int oi) {
-    if (s.flags[kFlagRoute] == op.layer + 1) return true;
+    if (s.flags[kFlagRoute] == route_tag(epoch, op.layer, p.L)) return true;
     const int E = p.E, k = p.top_k;
     float* r = s.act;  // [M][E]
     if (!wait_counter(op.aux_ctr, p.n_ctas, oi, 10)) return false;
@@ -1237,7 +1264,7 @@ struct Consumer {
         }
       rb->n_slots = n;
       __threadfence_block();
-      s.flags[kFlagRoute] = op.layer + 1;  // the producer lanes may now read the expert ids
+      s.flags[kFlagRoute] = route_tag(epoch, op.layer, p.L);  // the producer lanes may now read the ids
     }
     consumer_sync();
     if (blockIdx.x == 0) {  // a copy in global memory for inspection
@@ -2052,6 +2079,44 @@ __device__ __noinline__ bool attn_entry(const KParams& p, int oi, int pos, int M
   return ok;
 }
 
+// Consumers of a chained launch, between steps: the first thread waits (bounded) until the
+// step state's epoch moves past this CTA's copy, which the last CTA of the step writes after the
+// rest of the state, then copies the state in; every consumer thread learns the verdict.
+__device__ __noinline__ bool next_step_state(const KParams& p) {
+  bool ok = true;
+  consumer_sync();  // every consumer thread is done with the old copy
+  if (threadIdx.x == 0) {
+    const uint32_t want = g_st.epoch + 1u;
+    const volatile uint32_t* e = &p.state->epoch;
+    const uint64_t t0 = gtimer();
+    for (int it = 1; *e != want; ++it) {
+      if ((it & 15) == 0) {
+        if (aborted(p)) {
+          ok = false;
+          break;
+        }
+        if (gtimer() - t0 > p.timeout_ns) {
+          raise_error(p, DEC_ERR_TIMEOUT, -1, 0xFFFFFFFDu, *e, want, 14);
+          ok = false;
+          break;
+        }
+      }
+    }
+    if (ok) {
+      __threadfence();
+      const uint32_t* src = reinterpret_cast<const uint32_t*>(p.state);
+      uint32_t* dst = reinterpret_cast<uint32_t*>(&g_st);
+      // every other field first; the epoch last, which the producer lanes poll
+      constexpr int kEpochWord = (int)(offsetof(StepState, epoch) / 4);
+      for (int i = 0; i < (int)(sizeof(StepState) / 4); ++i)
+        if (i != kEpochWord) dst[i] = __ldcg(src + i);
+      __threadfence_block();
+      *reinterpret_cast<volatile uint32_t*>(&g_st.epoch) = __ldcg(src + kEpochWord);
+    }
+  }
+  return consumer_all(ok);
+}
+
 // ------------------------------------------------------------------ kernel
 __global__ void __launch_bounds__(kThreads, 1) dec_megakernel(const __grid_constant__ KParams p) {
   Smem s = carve(smem_raw, p);
@@ -2069,23 +2134,29 @@ __global__ void __launch_bounds__(kThreads, 1) dec_megakernel(const __grid_const
     mbar_init_fence();
   }
   __syncthreads();
-  const int pos = g_st.pos, M = g_st.m;
+  const int M = g_st.m;
   if (warp == kConsumerWarps) {
-    Producer pr{p, s, pos, M, l2_policy_evict_first()};
+    Producer pr{p, s, g_st.pos, M, l2_policy_evict_first(), g_st.epoch};
     pr.run(lane);
     return;
   }
-  // RoPE table of this call's positions (fp64 angle, then fp32 cos/sin).
-  for (int t = tid; t < M * 64; t += kConsumerThreads) {
-    const int m = t >> 6, i = t & 63;
-    const double inv = pow((double)p.rope_base, -2.0 * (double)i / 128.0);
-    double sn, cs;
-    sincos((double)(pos + m) * inv, &sn, &cs);
-    s.rope[t] = make_float2((float)cs, (float)sn);
+  for (int step = 0; step < steps_of(p); ++step) {
+    // later steps of a chained launch: wait for the step end the last CTA announces, then take
+    // the new state (its argmax as the token, the next position)
+    if (step > 0 && !next_step_state(p)) return;
+    const int pos = g_st.pos;
+    // RoPE table of this call's positions (fp64 angle, then fp32 cos/sin).
+    for (int t = tid; t < M * 64; t += kConsumerThreads) {
+      const int m = t >> 6, i = t & 63;
+      const double inv = pow((double)p.rope_base, -2.0 * (double)i / 128.0);
+      double sn, cs;
+      sincos((double)(pos + m) * inv, &sn, &cs);
+      s.rope[t] = make_float2((float)cs, (float)sn);
+    }
+    consumer_sync();
+    Consumer c(p);
+    if (!c.run(pos, M)) return;
   }
-  consumer_sync();
-  Consumer c(p);
-  c.run(pos, M);
 }
 
 }  // namespace decimpl
