@@ -1,7 +1,8 @@
 """Greedy generation chained inside one persistent launch (the monokernel): n steps, each
 feeding its argmax to the next at the next position, against the same steps launched one by
 one (which the other tests hold to the oracle). Tokens and the final logits agree bit for bit;
-one launch per chain. A one-layer MoE model routes the same layer in every step, so a stale
+one launch per chain; the last step's residual stream and the appended cache rows agree bit for
+bit. A one-layer MoE model routes the same layer in every step, so a stale
 routing from the previous step would show."""
 import numpy as np
 import pytest
@@ -32,15 +33,20 @@ def _chained_vs_stepwise(shape, seed, n, **kw):
     toks = a.generate(tok0, shape.kv_prefill, n)
     a.sync()
     assert a.launches() == 1
-    lg_chain = a.logits[0].cpu().numpy().copy()
+    hs_chain = a.hidden_stream().cpu().numpy().copy()
     b = decoder_for(shape, seed, cap, w=w, **kw)
     ref, tok = [], tok0
     for i in range(n):
         tok = b.step(tok, shape.kv_prefill + i)
         ref.append(tok)
     assert toks.cpu().tolist() == ref
-    # the chain's last step wrote the logits the stepwise run's last step wrote
-    assert np.array_equal(lg_chain, b.logits[0].cpu().numpy())
+    # the chain's last step left the residual stream (every block's output) the stepwise run's
+    # last step left, bit for bit; so are the cache rows both appended
+    assert np.array_equal(hs_chain, b.hidden_stream().cpu().numpy())
+    if shape.attn:
+        rows = slice(shape.kv_prefill, shape.kv_prefill + n)
+        assert np.array_equal(a.k_cache[:, :, rows].cpu().numpy(), b.k_cache[:, :, rows].cpu().numpy())
+        assert np.array_equal(a.v_cache[:, :, rows].cpu().numpy(), b.v_cache[:, :, rows].cpu().numpy())
     a.close()
     b.close()
 
