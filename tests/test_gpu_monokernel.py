@@ -1,9 +1,9 @@
 """Greedy generation chained inside one persistent launch (the monokernel): n steps, each
 feeding its argmax to the next at the next position, against the same steps launched one by
-one (which the other tests hold to the oracle). Tokens and the final logits agree bit for bit;
-one launch per chain; the last step's residual stream and the appended cache rows agree bit for
-bit. A one-layer MoE model routes the same layer in every step, so a stale
-routing from the previous step would show."""
+one (which the other tests hold to the oracle). The tokens agree, the chain takes one launch,
+and the last step's residual stream and the appended cache rows agree bit for bit. A one-layer
+MoE model routes the same layer in every step, so a stale routing from the previous step would
+show."""
 import numpy as np
 import pytest
 
