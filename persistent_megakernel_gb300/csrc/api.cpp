@@ -1,6 +1,7 @@
 // Host side of the C ABI declared in include/dec.h: config validation, workspace layout,
 // the step's op list, launch modes (persistent / per op / per-op CUDA graph) and the
 // sticky device status.
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -18,6 +19,9 @@ using namespace decimpl;
 
 #ifndef DEC_ATTN_SPLIT_DIV
 #define DEC_ATTN_SPLIT_DIV 1
+#endif
+#ifndef DEC_ATTN_TC
+#define DEC_ATTN_TC 1  // bf16 attention on the tensor cores, its tiles by TMA tensor copies
 #endif
 
 extern "C" cudaError_t dec_launch_megakernel(const KParams* kp, int cooperative, cudaStream_t stream);
@@ -104,6 +108,11 @@ bool validate(const dec_config* c, std::string& why) {
   if (c->kv_dtype != DEC_BF16 && c->kv_dtype != DEC_FP8_E4M3) return bad("kv_dtype must be DEC_BF16 or DEC_FP8_E4M3");
   if (!std::isfinite(c->rms_eps) || c->rms_eps < 0) return bad("rms_eps must be >= 0");
   return true;
+}
+
+// Attention runs on the tensor cores for a bf16 cache with at most 8 query heads per kv head.
+bool attn_tc_for(const dec_config* c) {
+  return DEC_ATTN_TC && c->n_q > 0 && c->kv_dtype == DEC_BF16 && c->n_q / c->n_kv <= 8;
 }
 
 int ctas_for(const dec_config* c) {
@@ -208,7 +217,9 @@ bool compute_layout(const dec_config* c, Layout& L, std::string& why) {
   act = align_up(act * 4, 256);
   const int common = dec_megakernel_common_bytes();
   const long long room = (long long)kSmemLimit - (long long)act - common;
-  long long slot = room / (kConsumerWarps * kStages) / 256 * 256;
+  // ring slots: 256-byte multiples, 1024 when tensor copies with a 128-byte swizzle land in them
+  const int slot_align = attn_tc_for(c) ? 1024 : 256;
+  long long slot = room / (kConsumerWarps * kStages) / slot_align * slot_align;
   slot = std::min<long long>(slot, kMaxSlotBytes);
   if (slot < 4096) {
     why = "shapes need more shared memory than a CTA has";
@@ -273,6 +284,10 @@ struct dec_ctx {
   bool sticky = false;
   dec_status sticky_code = DEC_OK;
   cudaGraphExec_t graph = nullptr;
+  int attn_tc = 0;                   // tensor-core attention (tensor maps below encoded)
+  const void* tmap_kc = nullptr;     // the caches the tensor maps describe
+  const void* tmap_vc = nullptr;
+  CUtensorMap tmap_k, tmap_v;
   int last_launches = 0;
   int drop_op = -1;  // failure injection: the next per-op call skips launching this op
 };
@@ -577,6 +592,9 @@ void fill_params(dec_ctx* c, KParams& k, size_t ops_off, int n_ops) {
   k.slot_bytes = L.slot_bytes;
   k.act_bytes = L.act_bytes;
   k.kv_fp8 = g.kv_dtype == DEC_FP8_E4M3 ? 1 : 0;
+  k.attn_tc = c->attn_tc;
+  k.tmap_k = c->tmap_k;
+  k.tmap_v = c->tmap_v;
   k.state = wsp<StepState>(c, L.state);
   k.status = wsp<Status>(c, L.status);
   k.tickets = wsp<uint32_t>(c, L.tickets);
@@ -603,10 +621,54 @@ void build_ops(dec_ctx* c) {
   fill_params(c, c->kp, c->lay.ops, (int)c->ops.size());
 }
 
+// The driver's tensor-map encoder, looked up once through the runtime (no link against the driver
+// library).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }();
+  return fn;
+}
+
+// Tensor maps of the bf16 key and value caches for tensor-core attention: each cache a 2D tensor
+// of 128 bf16 columns by (n_layers n_kv kv_capacity) rows of 256 bytes, read in boxes of 64
+// columns x kAttnTcRows rows with a 128-byte swizzle (the tensor-core tile's shared layout).
+dec_status ensure_tmaps(dec_ctx* c) {
+  const dec_config& g = c->cfg;
+  if (!attn_tc_for(&g)) {
+    c->attn_tc = 0;
+    return DEC_OK;
+  }
+  if (c->attn_tc && c->tmap_kc == c->kc && c->tmap_vc == c->vc) return DEC_OK;
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return fail(DEC_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t dims[2] = {(cuuint64_t)kHeadDim, (cuuint64_t)g.n_layers * g.n_kv * g.kv_capacity};
+  const cuuint64_t strides[1] = {(cuuint64_t)kHeadDim * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)kAttnTcRows};
+  const cuuint32_t estr[2] = {1, 1};
+  for (int which = 0; which < 2; ++which) {
+    CUresult r = enc(which ? &c->tmap_v : &c->tmap_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, which ? c->vc : c->kc, dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(DEC_ERR_CUDA, "encoding the KV cache tensor map failed (CUresult %d)", (int)r);
+  }
+  c->tmap_kc = c->kc;
+  c->tmap_vc = c->vc;
+  c->attn_tc = 1;
+  return DEC_OK;
+}
+
 dec_status prepare(dec_ctx* c) {
   if (c->sticky) return fail(DEC_ERR_STATE, "a device error is pending (code %d): call dec_reset", (int)c->sticky_code);
   if (!c->ops_dirty) return DEC_OK;
   dec_status st = check_weights(c);
+  if (st != DEC_OK) return st;
+  st = ensure_tmaps(c);
   if (st != DEC_OK) return st;
   build_ops(c);
   CUDA_TRY(cudaMemcpyAsync(c->ws + c->lay.ops, c->ops.data(), c->ops.size() * sizeof(OpDesc), cudaMemcpyHostToDevice,
@@ -947,6 +1009,8 @@ dec_status dec_run_layer(dec_ctx* c, int layer, const void* h_in, int m, int32_t
   if (g.n_q && (long long)pos + m > g.kv_capacity)
     return fail(DEC_ERR_CAPACITY, "positions %d..%d exceed kv_capacity %d", pos, pos + m - 1, g.kv_capacity);
   dec_status st = check_layer(c, layer);
+  if (st != DEC_OK) return st;
+  st = ensure_tmaps(c);
   if (st != DEC_OK) return st;
   std::vector<OpDesc> ops;
   ListBuilder b(c, ops, X_HIDDEN_IN);

@@ -14,6 +14,7 @@
 // (a fence would wait for the CTA's bulk copies in flight). Per-op arrival counters (relaxed
 // atomics) remain as a build option that gates the reads on a count instead.
 #pragma once
+#include <cuda.h>  // CUtensorMap (a type only: the library does not link the driver API)
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -36,6 +37,8 @@ constexpr int kPart = 132;                       // attention partial: max, sum,
 constexpr int kMaxSlotBytes = 16384;             // one warp's ring slot at most (attention rows <= 32)
 constexpr int kSmemLimit = 232448;               // dynamic shared memory per CTA on sm_103a
 constexpr int kNoAllocScratchBytes = 64 * 1024;  // static scratch of the allocation-free LM head
+constexpr int kAttnTcRows = 16;                  // KV rows of one tensor-core attention tile
+constexpr int kAttnTcBoxBytes = kAttnTcRows * 128;  // one 64-column box of a tile (swizzle span 128 B)
 
 enum OpType : int32_t {
   OP_QKV = 0,           // a = RMSNorm(x); qkv = W_qkv a
@@ -133,6 +136,10 @@ struct KParams {
   int32_t n_steps, pad2;              // greedy steps this launch runs (> 1: chained in the kernel)
   uint64_t* hs;                       // hidden stream, tagged [2L + 1][Mmax][H]
   uint64_t* trace;                    // DEC_TRACE builds: [n_ctas][n_ops][kTraceFields] %globaltimer stamps
+  int32_t attn_tc, pad3;              // 1: bf16 attention tiles come by TMA tensor copies (128-byte
+                                      // swizzle) and run on the tensor cores
+  CUtensorMap tmap_k, tmap_v;         // the bf16 key / value caches as 2D tensors: 128 columns x
+                                      // (L n_kv cap) rows, boxes of 64 columns x kAttnTcRows rows
 };
 
 // Trace record of one (CTA, op), DEC_TRACE builds only (compiled out otherwise):

@@ -249,6 +249,11 @@ __device__ __forceinline__ void token_group(int w, int M, int& m, int& gi, int& 
 
 __device__ __forceinline__ int bytes_per_col(int wtype) { return wtype == W_BF16 ? 2 : 1; }  // MXFP4: K/2 below
 
+// KV rows of one attention tile: fixed for tensor-core tiles, else what a ring slot holds.
+__device__ __forceinline__ int attn_rows(const KParams& p, int slot_bytes) {
+  return p.attn_tc ? kAttnTcRows : attn_rows_per_slot(slot_bytes, p.kv_fp8);
+}
+
 __device__ __forceinline__ int row_bytes(int wtype, int K) {
   return wtype == W_BF16 ? 2 * K : (wtype == W_FP8 ? K : K / 2);
 }
@@ -515,6 +520,19 @@ struct Producer {
   }
 
   __device__ __forceinline__ void copy_attn(const OpDesc* op, const Tile& t, uint8_t* dst, uint32_t fb) {
+    if (p.attn_tc) {
+      // four boxes of kAttnTcRows rows x 64 columns, 128-byte swizzle: keys 0-63, keys 64-127,
+      // values 0-63, values 64-127. Always whole boxes: rows past the tile belong to later
+      // positions (or, past the cache, are filled with zeros) and are masked by the consumer.
+      const int y = (__ldg(&op->layer) * p.n_kv + t.mat) * p.cap + t.r0;
+      mbar_expect_tx(fb, 4u * kAttnTcBoxBytes);
+      const uint32_t d = smem_addr(dst);
+      tma_load_2d(d, &p.tmap_k, 0, y, fb, policy);
+      tma_load_2d(d + kAttnTcBoxBytes, &p.tmap_k, 64, y, fb, policy);
+      tma_load_2d(d + 2 * kAttnTcBoxBytes, &p.tmap_v, 0, y, fb, policy);
+      tma_load_2d(d + 3 * kAttnTcBoxBytes, &p.tmap_v, 64, y, fb, policy);
+      return;
+    }
     const int rb = kv_row_bytes(p.kv_fp8);
     const uint32_t bytes = (uint32_t)(t.nr * rb);
     const size_t off = ((size_t)t.mat * p.cap + t.r0) * rb;  // bytes
@@ -586,7 +604,7 @@ struct Producer {
             if ((int32_t)(e - (epoch0 + (uint32_t)c.step)) < 0) return false;
             __threadfence_block();
           }
-          c.a.init(p, blockIdx.x, w, pos + c.step, M, attn_rows_per_slot(s.slot_bytes, p.kv_fp8));
+          c.a.init(p, blockIdx.x, w, pos + c.step, M, attn_rows(p, s.slot_bytes));
         } else {
           const int* experts = nullptr;
           int n_slots = 0;
@@ -890,6 +908,8 @@ __device__ __noinline__ bool copy_act_entry(const KParams& p, int oi, float* dst
                                             int src_stride, int cw);
 template <int G_>
 __device__ __noinline__ bool attn_entry(const KParams& p, int oi, int pos, int M);
+template <int G_>
+__device__ __noinline__ bool attn_tc_entry(const KParams& p, int oi, int r0, int r1, int m_tok, int M);
 
 // A consumer thread's view of the kernel. Built from scratch wherever it is needed (see
 // smem_raw), so out-of-line functions keep it in registers; the ring position of the thread's
@@ -1518,8 +1538,8 @@ struct Consumer {
       if (op.R <= 4) return gemv_tiles_entry<W_FP8, MT, 4, 0>(p, oi, op, M, xres, a, accd);
       return gemv_tiles_entry<W_FP8, MT, 8, 0>(p, oi, op, M, xres, a, accd);
     }
-    if constexpr (MT == 1)
-      if (whole && kw <= 32 * 3 * 32) return gemv_tiles_entry<W_MXFP4, 1, 8, 3>(p, oi, op, M, xres, a, accd);
+    // MXFP4 keeps its activations in shared memory: decoding is the bottleneck there, and a
+    // register copy would spill (measured: 10 % faster on the MoE stack)
     return gemv_tiles_entry<W_MXFP4, MT, 8, 0>(p, oi, op, M, xres, a, accd);
   }
 
@@ -1703,12 +1723,162 @@ struct Consumer {
     }
   }
 
+  // ---------------------------------------------------------------- attention on tensor cores
+  // One warp, token m_tok's G_ heads over the cached rows [r0, r1) of the current split, in
+  // tiles of kAttnTcRows rows that the producer brought by TMA with a 128-byte swizzle (keys in
+  // two 64-column boxes, then values in two). Scores S = Q K^T and outputs O = P V are warp-level
+  // bf16 MMAs (m16n8k16) with fp32 accumulation; the 16 rows of the A operand hold the G_ heads
+  // twice, as bf16 high parts (rows 0-7) and the bf16 rounding residues (rows 8-15), so q and p
+  // keep about 16 bits of mantissa and the two rows' products add up in fp32. Online softmax in
+  // base 2 on the score fragments; the state (max, sum, output) goes to the warp's merge slice.
+  template <int G_>
+  __device__ __forceinline__ bool attn_tc_t(int oi, int r0, int r1, int m_tok, int M) {
+    static_assert(G_ <= 8, "at most 8 query heads per kv head on the tensor-core path");
+    const int P = kAttnTcRows;
+    const AttnScratch a = attn_scratch(p, s, M, P);
+    const int g = lane >> 2, tq = lane & 3;
+    // Q fragments per 16-column step: rows g (high parts) and g + 8 (residues) of head g
+    uint32_t qf[8][4];
+    {
+      const float* qr = a.q + (m_tok * G_ + (g < G_ ? g : 0)) * 128;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const int d0 = 16 * kk + 2 * tq;
+        float x[4] = {qr[d0], qr[d0 + 1], qr[d0 + 8], qr[d0 + 9]};
+        if (g >= G_) x[0] = x[1] = x[2] = x[3] = 0.f;
+        float hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          hi[e] = __bfloat162float(__float2bfloat16_rn(x[e]));
+          lo[e] = x[e] - hi[e];
+        }
+        qf[kk][0] = pack_bf16x2(hi[0], hi[1]);
+        qf[kk][1] = pack_bf16x2(lo[0], lo[1]);
+        qf[kk][2] = pack_bf16x2(hi[2], hi[3]);
+        qf[kk][3] = pack_bf16x2(lo[2], lo[3]);
+      }
+    }
+    float o[16][4];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+    float mrun = -INFINITY, lrun = 0.f;
+    // this lane's row of the 8x8 matrices it addresses for ldmatrix, and its swizzle phase
+    const int mq = lane >> 3, rr = lane & 7;
+    const uint32_t koff = (uint32_t)(((mq >> 1) * 8 + rr) * 128);  // keys: matrices 2, 3 = rows 8-15
+    const uint32_t voff = (uint32_t)(((mq & 1) * 8 + rr) * 128);   // values: matrices 1, 3 = rows 8-15
+    bool ok = true;
+    for (int r = r0; r < r1; r += P) {
+      const int nr = min(P, r1 - r);
+      uint8_t* slot;
+      uint32_t eb;
+      if (!next_slot(oi, slot, eb)) {
+        ok = false;
+        break;
+      }
+      const uint32_t kb = smem_addr(slot), vb = kb + 2 * kAttnTcBoxBytes;
+      float sc4[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const int c = 2 * kk + (mq & 1);  // 16-byte column chunk of the 128 dims
+        uint32_t b[4];
+        ldsm_x4(kb + (uint32_t)((c >> 3) * kAttnTcBoxBytes) + koff + (uint32_t)((((c & 7) ^ rr)) << 4), b);
+        mma_bf16_16816(sc4[0], qf[kk], b[0], b[1]);
+        mma_bf16_16816(sc4[1], qf[kk], b[2], b[3]);
+      }
+      // scores of head g at rows 8j + 2 tq + e (high + residue rows), masked past the tile
+      float sv[2][2], mx = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int row = 8 * j + 2 * tq + e;
+          sv[j][e] = row < nr ? sc4[j][e] + sc4[j][2 + e] : -INFINITY;
+          mx = fmaxf(mx, sv[j][e]);
+        }
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const float mnew = fmaxf(mrun, mx);
+      const float scale = (mnew == -INFINITY) ? 1.f : (mrun == -INFINITY ? 0.f : exp2f(mrun - mnew));
+      float pv[2][2], psum = 0.f;
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          pv[j][e] = (sv[j][e] == -INFINITY) ? 0.f : exp2f(sv[j][e] - mnew);
+          psum += pv[j][e];
+        }
+      lrun = lrun * scale + psum;
+      mrun = mnew;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        o[j][0] *= scale;
+        o[j][1] *= scale;
+        o[j][2] *= scale;
+        o[j][3] *= scale;
+      }
+      uint32_t pf[4];
+      {
+        float hi[2][2], lo[2][2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            hi[j][e] = __bfloat162float(__float2bfloat16_rn(pv[j][e]));
+            lo[j][e] = pv[j][e] - hi[j][e];
+          }
+        pf[0] = pack_bf16x2(hi[0][0], hi[0][1]);
+        pf[1] = pack_bf16x2(lo[0][0], lo[0][1]);
+        pf[2] = pack_bf16x2(hi[1][0], hi[1][1]);
+        pf[3] = pack_bf16x2(lo[1][0], lo[1][1]);
+      }
+      if (nr < P) {
+        // value rows past the tile may hold anything the cache holds there: zero them, so a
+        // zero probability never meets a non-finite value
+        __syncwarp();
+        for (int i = lane; i < (P - nr) * 16; i += 32) {
+          const int row = nr + i / 16, ch = i % 16;
+          *reinterpret_cast<uint4*>(slot + 2 * kAttnTcBoxBytes + (ch >> 3) * kAttnTcBoxBytes + row * 128 +
+                                    ((ch & 7) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();  // the slot's next bulk fill comes after these writes
+        __syncwarp();
+      }
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+        const int c = 2 * jj + (mq >> 1);  // 16-byte column chunk: dims 8c .. 8c + 7
+        uint32_t b[4];
+        ldsm_x4_t(vb + (uint32_t)((c >> 3) * kAttnTcBoxBytes) + voff + (uint32_t)((((c & 7) ^ rr)) << 4), b);
+        mma_bf16_16816(o[2 * jj], pf, b[0], b[1]);
+        mma_bf16_16816(o[2 * jj + 1], pf, b[2], b[3]);
+      }
+      release(eb);
+    }
+    // the warp's state: head g's max, sum (its four lanes' parts) and output dims 8j + 2 tq + e
+    lrun += __shfl_xor_sync(0xffffffffu, lrun, 1);
+    lrun += __shfl_xor_sync(0xffffffffu, lrun, 2);
+    float* mgw = a.mg + warp * G_ * kPart;
+    if (g < G_) {
+      if (tq == 0) {
+        mgw[g * kPart] = mrun;
+        mgw[g * kPart + 1] = lrun;
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int d = 8 * j + 2 * tq;
+        mgw[g * kPart + 4 + d] = o[j][0] + o[j][2];
+        mgw[g * kPart + 4 + d + 1] = o[j][1] + o[j][3];
+      }
+    }
+    __syncwarp();
+    return ok;
+  }
+
   // ---------------------------------------------------------------- attention op
   template <int G_>
   __device__ __forceinline__ bool attn_op(int oi, const OpDesc& op, int pos, int M) {
     if (op.wait_ctr >= 0 && !wait_counter(op.wait_ctr, op.wait_n, oi, 4)) return false;
     if (tid == 0) TRACE(p, oi, 1, gtimer());
-    const int P = attn_rows_per_slot(s.slot_bytes, p.kv_fp8);
+    const int P = attn_rows(p, s.slot_bytes);
     const int rb = kv_row_bytes(p.kv_fp8);
     const int G = G_, MG = M * G, ns = p.ns_max;
     const AttnScratch a = attn_scratch(p, s, M, P);
@@ -1809,23 +1979,46 @@ struct Consumer {
       }
       float q[G_][16];
       const int sub = lane & 7;
+      auto load_q = [&]() {
 #pragma unroll
-      for (int h = 0; h < G_; ++h)
+        for (int h = 0; h < G_; ++h)
 #pragma unroll
-        for (int e = 0; e < 16; ++e) q[h][e] = a.q[(m_tok * G + h) * 128 + sub * 16 + e] * sk;
+          for (int e = 0; e < 16; ++e) q[h][e] = a.q[(m_tok * G + h) * 128 + sub * 16 + e] * sk;
+      };
       Tile t;
-      while (it.next_in_split(t)) {
-        uint8_t* slot;
-        uint32_t eb;
-        if (!next_slot(oi, slot, eb)) {
-          ok = false;
-          break;
+      if (p.attn_tc) {
+        // the cached rows on the tensor cores (out of line); the warp's state comes back
+        // through its slice of the merge scratch
+        if (it.fresh) it.enter_split();
+        save_tiles();
+        if (!attn_tc_entry<G_>(p, oi, it.q, it.qe, m_tok, M)) ok = false;
+        n_tiles = s.ntiles[warp];
+        it.q = it.qe;
+        load_q();  // for this call's own rows, after the call (nothing to keep live across it)
+        const float* mgw = a.mg + warp * G * kPart;
+#pragma unroll
+        for (int h = 0; h < G_; ++h) {
+          A.mrun[h] = mgw[h * kPart];
+          A.lrun[h] = mgw[h * kPart + 1];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) A.o[h][e] = mgw[h * kPart + 4 + lane * 4 + e];
         }
-        if (p.kv_fp8)
-          attn_warp_tile<G_, true>(A, q, slot, slot + t.nr * rb, t.nr, -1, m_tok, sc, P, lane);
-        else
-          attn_warp_tile<G_, false>(A, q, slot, slot + t.nr * rb, t.nr, -1, m_tok, sc, P, lane);
-        release(eb);
+        __syncwarp();
+      } else {
+        load_q();
+        while (it.next_in_split(t)) {
+          uint8_t* slot;
+          uint32_t eb;
+          if (!next_slot(oi, slot, eb)) {
+            ok = false;
+            break;
+          }
+          if (p.kv_fp8)
+            attn_warp_tile<G_, true>(A, q, slot, slot + t.nr * rb, t.nr, -1, m_tok, sc, P, lane);
+          else
+            attn_warp_tile<G_, false>(A, q, slot, slot + t.nr * rb, t.nr, -1, m_tok, sc, P, lane);
+          release(eb);
+        }
       }
       // this call's own rows: the first warp of each token group attends to them (causally)
       if (ok && gi == 0 && nn > 0) {
@@ -2075,6 +2268,14 @@ template <int G_>
 __device__ __noinline__ bool attn_entry(const KParams& p, int oi, int pos, int M) {
   Consumer c(p);
   const bool ok = c.attn_op<G_>(oi, *c.s.op, pos, M);
+  c.save_tiles();
+  return ok;
+}
+
+template <int G_>
+__device__ __noinline__ bool attn_tc_entry(const KParams& p, int oi, int r0, int r1, int m_tok, int M) {
+  Consumer c(p);
+  const bool ok = c.attn_tc_t<G_>(oi, r0, r1, m_tok, M);
   c.save_tiles();
   return ok;
 }

@@ -105,3 +105,39 @@ def test_teacher_forced_layers_along_chain(setup):
             assert am == int(np.argmax(lg_ref)), (p, am, int(np.argmax(lg_ref)))
         tok = am
         done = p + 1
+
+
+def test_verify_window_full_size(setup):
+    """A 4-token verify window at positions 4096..4099 of the full-size decoder (the model's own
+    greedy token first, then three drafts: two of the oracle's greedy continuation and one wrong
+    one), in a context with max_verify 4 over the same weights: logits of every position within
+    tolerance of the oracle's causal steps, the argmax where the top-2 gap is safe, the accepted
+    prefix."""
+    s, seed, dec, orc = setup
+    from persistent_megakernel_gb300 import binding as B
+    from persistent_megakernel_gb300.model import make_config
+    import torch
+    pos0 = s.kv_prefill
+    tok0 = synth.start_token(seed, s.vocab)
+    greedy = [inf["token"] for inf in orc.greedy(tok0, pos0, 3)]
+    wrong = (greedy[2] + 1) % s.vocab
+    toks = [tok0, greedy[0], greedy[1], wrong]
+    infos, n_acc = orc.verify(toks, pos0)
+    cfg = make_config(s, dec.capacity, 4)
+    nbytes = B.dec_workspace_bytes(cfg)
+    ws_all = torch.zeros(nbytes + 256, dtype=torch.uint8, device=dec.device)
+    off = (-ws_all.data_ptr()) % 256
+    torch.cuda.synchronize()
+    ctx = B.dec_init(cfg, dec.stream.cuda_stream, ws_all[off:off + nbytes])
+    B.dec_load_weights(ctx, dec._tensors)
+    B.dec_set_kv_cache(ctx, dec.k_cache, dec.v_cache)
+    logits = torch.empty((4, s.vocab), dtype=torch.float32, device=dec.device)
+    am, acc = B.dec_verify(ctx, toks, None, 4, pos0, logits)
+    lg = logits.cpu().numpy()
+    for i in range(4):
+        ref = infos[i]["logits"]
+        assert rel_err(lg[i], ref) <= TOL, (i, rel_err(lg[i], ref))
+        if top2_margin(ref) > 1e-4 * np.max(np.abs(ref)):
+            assert am[i] == infos[i]["token"], (i, am[i], infos[i]["token"])
+    assert acc == n_acc, (acc, n_acc)
+    B.dec_free(ctx)

@@ -10,6 +10,7 @@
    (at least 3 of every 4 layer-steps must be checked; the others are reported as ambiguous);
    the logits of every checked step against the oracle's FP8 head applied to the GPU's final
    hidden state, and the argmax where the top-2 gap is safe.
+4. A 4-token verify window of the full stack, teacher-forced per sampled layer and position.
 """
 import numpy as np
 import pytest
@@ -163,5 +164,54 @@ def test_moe_stack_full_teacher_forced(built):
     _check_step(dec, s, head, orcs, tok, s.kv_prefill + LAST, LAST, counts)
     n = (STEPS + 1) * len(LAYERS)
     print(f"top-k checked exactly on {counts['checked']} of {n} layer-steps, {counts['ambiguous']} ambiguous")
+    assert counts["checked"] >= 3 * n // 4, counts
+    dec.close()
+
+
+def test_moe_stack_full_verify_window(built):
+    """A 4-token verify window of the full stack at positions 32768..32771 (a context with
+    max_verify 4), teacher-forced per sampled layer: the oracle takes each position in turn,
+    causally, over the prefill plus the window's earlier rows as the GPU wrote them; every block
+    output within tolerance, top-k exact wherever the oracle's gap is safe (3 of 4 at least),
+    and every position's logits against the oracle's FP8 head."""
+    from tests.device_inputs import device_decoder
+    s = synth.moe_stack_shape()
+    dec = device_decoder(s, SEED, s.kv_prefill + 8, max_verify=4)
+    head = _Head(s)
+    orcs = {l: _layer_oracle(s, l) for l in LAYERS}
+    tok0 = synth.start_token(SEED, s.vocab)
+    toks = [tok0] + [int(x) for x in synth.bits(SEED, synth.tensor_id("token", 0, 1), 3) % np.uint64(s.vocab)]
+    pos = s.kv_prefill
+    am, _ = dec.verify(toks, pos)
+    hs = dec.hidden_stream().cpu().numpy().astype(np.float64)  # [2L + 1][4][H]
+    kc = {l: dec.k_cache[l, :, pos:pos + 4].cpu().numpy().view(np.uint16) for l in LAYERS}
+    vc = {l: dec.v_cache[l, :, pos:pos + 4].cpu().numpy().view(np.uint16) for l in LAYERS}
+    counts = {"checked": 0, "ambiguous": 0}
+    for m in range(4):
+        for l in LAYERS:
+            orc = orcs[l]
+            if m > 0:  # the window's earlier rows, as the GPU appended them
+                orc.K[0][:, pos:pos + m] = kc[l][:, :m]
+                orc.V[0][:, pos:pos + m] = vc[l][:, :m]
+            x_in = bf16_to_f64_fast(head.embed[toks[m]]) if l == 0 else hs[2 * l, m]
+            y = orc.attention_block(0, x_in, pos + m)
+            assert rel_err(hs[2 * l + 1, m], y) <= TOL, (m, l, "attention", rel_err(hs[2 * l + 1, m], y))
+            info = {}
+            z = orc.ffn_block(0, hs[2 * l + 1, m], info)
+            assert rel_err(hs[2 * l + 2, m], z) <= TOL, (m, l, "moe", rel_err(hs[2 * l + 2, m], z))
+            got = dec.routing(l)["topk"][m][: s.top_k].tolist()
+            if _router_gap(orc, hs[2 * l + 1, m]) > ROUTER_MARGIN:
+                assert got == [int(e) for e in info["topk"][0]], (m, l, got, info["topk"][0])
+                counts["checked"] += 1
+            else:
+                counts["ambiguous"] += 1
+        lg_ref = head.logits(hs[2 * s.n_layers, m])
+        lg = dec.logits[m].cpu().numpy()
+        assert rel_err(lg, lg_ref) <= TOL, (m, rel_err(lg, lg_ref))
+        if top2_margin(lg_ref) > 1e-3 * np.max(np.abs(lg_ref)):
+            assert am[m] == ops.argmax_first(lg_ref), (m, am[m], ops.argmax_first(lg_ref))
+    n = 4 * len(LAYERS)
+    print(f"verify window: top-k checked exactly on {counts['checked']} of {n} layer-positions, "
+          f"{counts['ambiguous']} ambiguous")
     assert counts["checked"] >= 3 * n // 4, counts
     dec.close()
