@@ -128,16 +128,21 @@ class OracleModel:
         q = ops.rope(q, pos, s.rope_base)
         k = ops.rope(k, pos, s.rope_base)
         # the cache holds bf16 (or FP8 codes): the new row is stored rounded, then read back (R4)
+        # sliding-window attention (Muse Spark Open megakernel article: most of that model's layers
+        # attend over the last 2,048 tokens only): the token at pos sees positions
+        # pos - W + 1 .. pos; W = 0 is global attention over 0 .. pos
+        W = getattr(s, "attn_window", 0)
+        lo = max(0, pos - W + 1) if W > 0 else 0
         if self.kv_fp8:
             self.K[l][:, pos] = F.quantize_kv_fp8(k, self._kv_scale(l, 0, 2))
             self.V[l][:, pos] = F.quantize_kv_fp8(v, self._kv_scale(l, 1, 2))
-            Kc = F.dequant_kv_fp8(self.K[l][:, : pos + 1], self._kv_scale(l, 0, 3))
-            Vc = F.dequant_kv_fp8(self.V[l][:, : pos + 1], self._kv_scale(l, 1, 3))
+            Kc = F.dequant_kv_fp8(self.K[l][:, lo: pos + 1], self._kv_scale(l, 0, 3))
+            Vc = F.dequant_kv_fp8(self.V[l][:, lo: pos + 1], self._kv_scale(l, 1, 3))
         else:
             self.K[l][:, pos] = F.f64_to_bf16(k)
             self.V[l][:, pos] = F.f64_to_bf16(v)
-            Kc = bf16_to_f64_fast(self.K[l][:, : pos + 1])
-            Vc = bf16_to_f64_fast(self.V[l][:, : pos + 1])
+            Kc = bf16_to_f64_fast(self.K[l][:, lo: pos + 1])
+            Vc = bf16_to_f64_fast(self.V[l][:, lo: pos + 1])
         o = ops.attention(q, Kc, Vc)
         return x + ops.gemv(self.w(l, "w_o"), o.reshape(-1))
 

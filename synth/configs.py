@@ -30,6 +30,7 @@ class ModelShape:
     kv_prefill: int = 0     # cached positions before the first decode step
     lm_head_dtype: str = "bf16"   # "bf16" | "fp8"
     kv_dtype: str = "bf16"        # "bf16" | "fp8" (e4m3 codes with a scale per layer, K/V and kv head)
+    attn_window: int = 0          # > 0: every query attends to the last attn_window positions only
     embedding: bool = False       # True: the step starts from E[token]; False: from a given hidden
     final_norm: bool = True       # RMSNorm before the LM head
     steps: int = 1                # greedy decode steps of the workload

@@ -80,13 +80,15 @@ class LoopModel:
                 self.V[l][g].append([rb(t) for t in v])
                 assert len(self.K[l][g]) == pos + 1
             o = []
+            lo = max(0, pos - s.attn_window + 1) if s.attn_window else 0  # the window's first position
             for h in range(s.n_q):
                 g = h * s.n_kv // s.n_q
-                sc = [sum(q[h][i] * kk[i] for i in range(d)) / math.sqrt(d) for kk in self.K[l][g]]
+                keys, vals = self.K[l][g][lo:], self.V[l][g][lo:]
+                sc = [sum(q[h][i] * kk[i] for i in range(d)) / math.sqrt(d) for kk in keys]
                 m = max(sc)
                 z = [math.exp(t - m) for t in sc]
                 tot = sum(z)
-                o += [sum(z[j] / tot * self.V[l][g][j][i] for j in range(len(z))) for i in range(d)]
+                o += [sum(z[j] / tot * vals[j][i] for j in range(len(z))) for i in range(d)]
             Wo = [f(r) for r in w["w_o"]]
             x = [x[i] + y for i, y in enumerate(mv(Wo, o))]
             hid.append(x)
@@ -189,4 +191,29 @@ def test_pos0_attention_returns_v():
     o = np.concatenate([v[ops.kv_group(h, s.n_q, s.n_kv)] for h in range(s.n_q)])
     x0 = om.embed(2)
     want = x0 + om.w(0, "w_o") @ o
+    assert np.allclose(inf["hidden"][0], want, rtol=1e-13)
+
+
+def test_sliding_window_matches_loop_evaluation():
+    # every token attends to its last 2 positions only (prefill 3, so the window cuts the cache)
+    _compare(TINY_DENSE.with_(attn_window=2), 7, 3)
+
+
+def test_sliding_window_special_cases():
+    s = TINY_DENSE.with_(n_layers=1)
+    pos = s.kv_prefill + 1
+    # a window covering every position is global attention, bit for bit
+    a = _oracle(s, 8, pos + 2)
+    b = _oracle(s.with_(attn_window=pos + 1), 8, pos + 2)
+    for p in (s.kv_prefill, pos):
+        assert np.array_equal(a.step_token(3, p)["logits"], b.step_token(3, p)["logits"])
+    # a window of one position: attention returns the token's own (bf16) value
+    from oracle import ops
+    from oracle.model import bf16_to_f64_fast
+    w1 = s.with_(attn_window=1)
+    om = _oracle(w1, 9, pos + 1)
+    inf = om.step_token(2, s.kv_prefill)
+    v = bf16_to_f64_fast(om.V[0][:, s.kv_prefill])
+    o = np.concatenate([v[ops.kv_group(h, s.n_q, s.n_kv)] for h in range(s.n_q)])
+    want = om.embed(2) + om.w(0, "w_o") @ o
     assert np.allclose(inf["hidden"][0], want, rtol=1e-13)
