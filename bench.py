@@ -234,6 +234,19 @@ def cpu_baseline(s, layers, head, kv, seed):
                       f"{dt:.2f} s per step"}
 
 
+def cpu_baseline_one_core(workload: str, seed: int):
+    """The oracle's layer sample (cpu_baseline_layer) on one host core: a child process pinned to
+    one core with every BLAS / OpenMP pool at one thread (set before numpy loads)."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               BLIS_NUM_THREADS="1", NUMEXPR_NUM_THREADS="1")
+    try:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-one-core", "--workload", workload,
+                            "--seed", str(seed)], env=env, capture_output=True, text=True, timeout=300)
+        return json.loads(r.stdout.strip().splitlines()[-1])
+    except Exception as e:  # reported, never fatal to the bench line
+        return {"error": f"one-core sample failed: {type(e).__name__}"}
+
+
 def run_reference(args):
     """Reference arm: the CPU oracle on the same workload; each step = one decoder layer of one
     token (dense 2B: attention + FFN of layer i mod 4 at position 4096 + i mod 256, the 28 layers
@@ -389,10 +402,15 @@ def main():
     ap.add_argument("--verify", type=int, default=1, choices=[1, 2, 3, 4],
                     help="> 1: time verify windows of this many tokens")
     ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"], help="KV cache format (fp8: e4m3, scales 1.0)")
+    ap.add_argument("--cpu-one-core", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling captures only: fewer decoder layers (the line is then not the workload's)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.cpu_one_core:  # child of cpu_baseline_one_core: the oracle's layer sample on one core
+        os.sched_setaffinity(0, {sorted(os.sched_getaffinity(0))[0]})
+        print(json.dumps(cpu_baseline_layer(workload_shape(args.workload), args.seed)))
+        return
     if args.impl == "reference":
         return run_reference(args)
 
@@ -473,6 +491,7 @@ def main():
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(s, layers, head, kv, args.seed) if layers is not None else cpu_baseline_layer(s, args.seed)
+        cpu["one_core"] = cpu_baseline_one_core(args.workload, args.seed)
 
     if rank == 0:
         line = {

@@ -86,6 +86,9 @@ typedef struct {
   uint64_t spin_timeout_ns; /* limit of every device wait (0: 2 s) */
   int num_ctas;      /* persistent CTAs (0: one per SM) */
   dec_dtype kv_dtype; /* KV cache: DEC_BF16 (0) or DEC_FP8_E4M3 */
+  int attn_window;   /* 0: global attention; W > 0: the token at position p attends to positions
+                        p - W + 1 .. p only (sliding-window attention, the Muse Spark Open megakernel
+                        article, section "where the kernel boundary sits"), W >= max_verify */
 } dec_config;
 
 typedef struct dec_ctx dec_ctx;

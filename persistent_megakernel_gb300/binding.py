@@ -48,7 +48,8 @@ class DecConfig(ctypes.Structure):
         "vocab", "kv_capacity", "max_verify", "embedding", "final_norm")] + [
         ("rms_eps", ctypes.c_float), ("rope_base", ctypes.c_float),
         ("lm_head_dtype", ctypes.c_int), ("expert_dtype", ctypes.c_int), ("mode", ctypes.c_int),
-        ("spin_timeout_ns", ctypes.c_uint64), ("num_ctas", ctypes.c_int), ("kv_dtype", ctypes.c_int)]
+        ("spin_timeout_ns", ctypes.c_uint64), ("num_ctas", ctypes.c_int), ("kv_dtype", ctypes.c_int),
+        ("attn_window", ctypes.c_int)]
 
 
 class DecTensor(ctypes.Structure):

@@ -70,7 +70,7 @@ struct LayerW {
 constexpr int kMaxSubOps = 8;  // ops of one layer (at most 7) or of the LM head alone
 
 struct Layout {  // byte offsets into the workspace
-  size_t state, status, tickets, ctr, ops, subops, hs, qkv, attn_out, hbuf, rlogits, route, eh, part, logits, am_val, am_idx,
+  size_t state, status, tickets, ctr, ops, subops, wops, tmaps, hs, qkv, attn_out, hbuf, rlogits, route, eh, part, logits, am_val, am_idx,
       am_out, trace, total;
   int n_ops, n_tickets, n_ctas, ns_max, slot_bytes, act_bytes, exp_stage_all;
 };
@@ -106,6 +106,8 @@ bool validate(const dec_config* c, std::string& why) {
   if (c->mode < DEC_MODE_PERSISTENT || c->mode > DEC_MODE_PER_OP_GRAPH) return bad("bad mode");
   if (c->num_ctas < 0) return bad("num_ctas must be >= 0");
   if (c->kv_dtype != DEC_BF16 && c->kv_dtype != DEC_FP8_E4M3) return bad("kv_dtype must be DEC_BF16 or DEC_FP8_E4M3");
+  if (c->attn_window < 0 || (c->attn_window > 0 && c->attn_window < c->max_verify))
+    return bad("attn_window must be 0 (global) or at least max_verify");
   if (!std::isfinite(c->rms_eps) || c->rms_eps < 0) return bad("rms_eps must be >= 0");
   return true;
 }
@@ -188,19 +190,21 @@ bool compute_layout(const dec_config* c, Layout& L, std::string& why) {
   L.ns_max = c->n_q ? std::max(1, C / c->n_kv / DEC_ATTN_SPLIT_DIV) : 1;
   L.n_tickets = 2;  // LM-head argmax, step end
 
-  // shared-memory scratch ("act") the largest op needs, in floats
+  // shared-memory scratch ("act") the largest op needs, in floats; a multi-token list's
+  // tensor-core ops stage their inputs in kMmax tokens' bytes whatever the window
   const int rows_cta = (H + C - 1) / C + 16;
-  size_t act = (size_t)M * H;
+  const int Ma = M > 1 ? kMmax : 1;
+  size_t act = (size_t)Ma * H;
   act = std::max(act, (size_t)2 * kConsumerThreads);
   if (c->n_q) {
     const size_t MG = (size_t)M * G;
-    act = std::max(act, (size_t)M * c->n_q * kHeadDim + (size_t)rows_cta * M * (1 + kConsumerWarps));
+    act = std::max(act, (size_t)Ma * c->n_q * kHeadDim + (size_t)rows_cta * M * (1 + kConsumerWarps));
     // the attention scratch the kernel carves (at most 32 KV rows per ring slot)
     (void)MG;
     act = std::max(act, (size_t)attn_layout(M, G, kMaxSlotBytes / 512, L.ns_max).end);
   }
-  if (c->ffn) act = std::max(act, (size_t)M * c->ffn + (size_t)rows_cta * M * (1 + kConsumerWarps));
-  act = std::max(act, (size_t)M * H + (size_t)2 * (rows_cta + 1) * M * kConsumerWarps);  // column-split partials
+  if (c->ffn) act = std::max(act, (size_t)Ma * c->ffn + (size_t)rows_cta * M * (1 + kConsumerWarps));
+  act = std::max(act, (size_t)Ma * H + (size_t)2 * (rows_cta + 1) * M * kConsumerWarps);  // column-split partials
   L.exp_stage_all = 0;
   if (c->n_experts) {
     act = std::max(act, (size_t)M * c->n_experts);
@@ -218,7 +222,7 @@ bool compute_layout(const dec_config* c, Layout& L, std::string& why) {
   const int common = dec_megakernel_common_bytes();
   const long long room = (long long)kSmemLimit - (long long)act - common;
   // ring slots: 256-byte multiples, 1024 when tensor copies with a 128-byte swizzle land in them
-  const int slot_align = attn_tc_for(c) ? 1024 : 256;
+  const int slot_align = (attn_tc_for(c) || c->max_verify > 1) ? 1024 : 256;
   long long slot = room / (kConsumerWarps * kStages) / slot_align * slot_align;
   slot = std::min<long long>(slot, kMaxSlotBytes);
   if (slot < 4096) {
@@ -240,6 +244,9 @@ bool compute_layout(const dec_config* c, Layout& L, std::string& why) {
   L.ctr = take((size_t)(std::max(1, L.n_ops) + (c->n_q ? nl * c->n_kv : 0)) * 4);
   L.ops = take((size_t)std::max(1, L.n_ops) * sizeof(OpDesc));
   L.subops = take((size_t)kMaxSubOps * sizeof(OpDesc));  // a layer or the LM head run on its own
+  // multi-token calls (max_verify > 1): their own op list, and a tensor map per tensor-core op
+  L.wops = take((size_t)(c->max_verify > 1 ? std::max(1, L.n_ops) : 0) * sizeof(OpDesc));
+  L.tmaps = take((size_t)(c->max_verify > 1 ? std::max(1, L.n_ops) : 0) * sizeof(CUtensorMap));
   // activations handed between CTAs are tagged 8-byte words (see ptx.cuh), one buffer per
   // layer so that no word is written twice in a step
   L.hs = take((size_t)(2 * nl + 1) * M * H * 8);
@@ -285,6 +292,9 @@ struct dec_ctx {
   dec_status sticky_code = DEC_OK;
   cudaGraphExec_t graph = nullptr;
   int attn_tc = 0;                   // tensor-core attention (tensor maps below encoded)
+  std::vector<OpDesc> wops;          // the op list of multi-token calls (max_verify > 1)
+  KParams wkp;
+  std::vector<CUtensorMap> tmaps_host;  // the tensor maps of its tensor-core ops
   const void* tmap_kc = nullptr;     // the caches the tensor maps describe
   const void* tmap_vc = nullptr;
   CUtensorMap tmap_k, tmap_v;
@@ -328,6 +338,20 @@ dec_status check_weights(dec_ctx* c) {
   return check_head(c);
 }
 
+// The driver's tensor-map encoder, looked up once through the runtime (no link against the driver
+// library).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }();
+  return fn;
+}
+
 constexpr int kLmHeadTicket = 0;  // tickets: the LM head's argmax, then the step end
 constexpr int kStepTicket = 1;
 
@@ -338,6 +362,8 @@ struct ListBuilder {
   dec_ctx* c;
   std::vector<OpDesc>& ops;
   int xsrc, x_idx, prev;
+  bool window = false;               // a multi-token list: bf16 matrices on tensor-core tiles
+  dec_status err = DEC_OK;
 
   ListBuilder(dec_ctx* c_, std::vector<OpDesc>& ops_, int xsrc_) : c(c_), ops(ops_), xsrc(xsrc_), x_idx(0), prev(-1) {}
 
@@ -356,9 +382,31 @@ struct ListBuilder {
     return o;
   }
 
-  void geom(OpDesc& o) const {
+  void geom(OpDesc& o) {
     const Layout& L = c->lay;
     const int M = c->cfg.max_verify;
+    if (window && o.wtype == W_BF16 && o.K % 64 == 0 && o.N % kGemvTcRows == 0 &&
+        L.slot_bytes >= kGemvTcRows * 2 * 64) {
+      // tensor-core tiles: kGemvTcRows rows x Kc columns in boxes of 64 columns (128-byte swizzle)
+      o.tc = 1;
+      o.R = kGemvTcRows;
+      o.unit = kGemvTcRows;
+      int kc = (L.slot_bytes / (kGemvTcRows * 2 * 64)) * 64;
+      o.Kc = std::min(o.K, kc);
+      o.csplit = 0;
+      o.kw = 0;
+      // fewer row groups per CTA than warps: split the columns across the warps instead (the
+      // partial sums of the CTA's rows must fit next to the staged inputs)
+      const int C = L.n_ctas, groups = (o.N / kGemvTcRows + C - 1) / C;
+      const size_t parts = (size_t)kConsumerWarps * groups * kGemvTcRows * M;
+      const size_t staged = (size_t)kMmax * o.K + (o.type == OP_OPROJ || o.type == OP_DOWN ? (size_t)groups * kGemvTcRows * M : 0);
+      if (o.type != OP_LMHEAD && groups < kConsumerWarps && (staged + parts) * 4 <= (size_t)L.act_bytes) {
+        o.csplit = 1;
+        o.kw = ((o.K + kConsumerWarps - 1) / kConsumerWarps + 63) / 64 * 64;
+      }
+      encode_tmap(o);
+      return;
+    }
     tile_geometry(o.wtype, o.K, o.pair, L.slot_bytes, M, o.R, o.Kc, o.unit);
     // rows too wide for one slot (or for activations in registers): split the columns across
     // the CTA's warps instead of its rows (bf16 / FP8 matrices without expert slots)
@@ -376,6 +424,28 @@ struct ListBuilder {
         o.R = r / o.unit * o.unit;
       }
     }
+  }
+
+  // The op's bf16 weight matrix as a 2D tensor map (K columns x N rows, boxes of 64 columns x
+  // kGemvTcRows rows, 128-byte swizzle), kept on the host and uploaded with the list.
+  void encode_tmap(OpDesc& o) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    CUtensorMap m;
+    std::memset(&m, 0, sizeof(m));
+    if (!enc) {
+      err = fail(DEC_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    } else {
+      const cuuint64_t dims[2] = {(cuuint64_t)o.K, (cuuint64_t)o.N};
+      const cuuint64_t strides[1] = {(cuuint64_t)o.K * 2};
+      const cuuint32_t box[2] = {64, (cuuint32_t)kGemvTcRows};
+      const cuuint32_t estr[2] = {1, 1};
+      const CUresult r = enc(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(o.w), dims, strides, box, estr,
+                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      if (r != CUDA_SUCCESS) err = fail(DEC_ERR_CUDA, "encoding a weight tensor map failed (CUresult %d)", (int)r);
+    }
+    o.tmap = reinterpret_cast<const CUtensorMap*>(c->ws + c->lay.tmaps) + c->tmaps_host.size();
+    c->tmaps_host.push_back(m);
   }
 
   uint64_t* hs_at(int idx) const {  // tagged [Mmax][H]
@@ -593,6 +663,7 @@ void fill_params(dec_ctx* c, KParams& k, size_t ops_off, int n_ops) {
   k.act_bytes = L.act_bytes;
   k.kv_fp8 = g.kv_dtype == DEC_FP8_E4M3 ? 1 : 0;
   k.attn_tc = c->attn_tc;
+  k.attn_window = g.attn_window;
   k.tmap_k = c->tmap_k;
   k.tmap_v = c->tmap_v;
   k.state = wsp<StepState>(c, L.state);
@@ -612,27 +683,26 @@ void fill_params(dec_ctx* c, KParams& k, size_t ops_off, int n_ops) {
 }
 
 // The whole step: every layer, then the LM head.
-void build_ops(dec_ctx* c) {
+dec_status build_ops(dec_ctx* c) {
   const dec_config& g = c->cfg;
   c->ops.clear();
   ListBuilder b(c, c->ops, g.embedding ? X_EMBED : X_HIDDEN_IN);
   for (int l = 0; l < g.n_layers; ++l) b.layer(l);
   if (g.vocab) b.head(wsp<float>(c, c->lay.logits));
   fill_params(c, c->kp, c->lay.ops, (int)c->ops.size());
-}
-
-// The driver's tensor-map encoder, looked up once through the runtime (no link against the driver
-// library).
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      f = nullptr;
-    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  }();
-  return fn;
+  // multi-token calls: the same step with the bf16 matrices on tensor-core tiles (one-token
+  // calls keep the CUDA-core list above)
+  c->wops.clear();
+  c->tmaps_host.clear();
+  if (g.max_verify > 1) {
+    ListBuilder w(c, c->wops, g.embedding ? X_EMBED : X_HIDDEN_IN);
+    w.window = true;
+    for (int l = 0; l < g.n_layers; ++l) w.layer(l);
+    if (g.vocab) w.head(wsp<float>(c, c->lay.logits));
+    if (w.err != DEC_OK) return w.err;
+    fill_params(c, c->wkp, c->lay.wops, (int)c->wops.size());
+  }
+  return DEC_OK;
 }
 
 // Tensor maps of the bf16 key and value caches for tensor-core attention: each cache a 2D tensor
@@ -640,7 +710,9 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // columns x kAttnTcRows rows with a 128-byte swizzle (the tensor-core tile's shared layout).
 dec_status ensure_tmaps(dec_ctx* c) {
   const dec_config& g = c->cfg;
-  if (!attn_tc_for(&g)) {
+  // a tile of keys and values (four boxes) must fit a ring slot: large multi-token staging
+  // areas leave smaller slots, and those contexts keep the CUDA-core attention tiles
+  if (!attn_tc_for(&g) || c->lay.slot_bytes < 4 * kAttnTcBoxBytes) {
     c->attn_tc = 0;
     return DEC_OK;
   }
@@ -670,9 +742,16 @@ dec_status prepare(dec_ctx* c) {
   if (st != DEC_OK) return st;
   st = ensure_tmaps(c);
   if (st != DEC_OK) return st;
-  build_ops(c);
+  st = build_ops(c);
+  if (st != DEC_OK) return st;
   CUDA_TRY(cudaMemcpyAsync(c->ws + c->lay.ops, c->ops.data(), c->ops.size() * sizeof(OpDesc), cudaMemcpyHostToDevice,
                            c->stream));
+  if (!c->wops.empty()) {
+    CUDA_TRY(cudaMemcpyAsync(c->ws + c->lay.wops, c->wops.data(), c->wops.size() * sizeof(OpDesc),
+                             cudaMemcpyHostToDevice, c->stream));
+    CUDA_TRY(cudaMemcpyAsync(c->ws + c->lay.tmaps, c->tmaps_host.data(), c->tmaps_host.size() * sizeof(CUtensorMap),
+                             cudaMemcpyHostToDevice, c->stream));
+  }
   CUDA_TRY(cudaStreamSynchronize(c->stream));
   if (c->graph) {
     cudaGraphExecDestroy(c->graph);
@@ -787,7 +866,8 @@ dec_status run_call(dec_ctx* c, int32_t pos, int m, const int32_t* tokens, const
   if (st != DEC_OK) return st;
   st = write_state(c, pos, m, tokens, hidden, 0, nullptr);
   if (st != DEC_OK) return st;
-  st = launch_list(c, c->kp, true);
+  // several tokens: the multi-token list (bf16 matrices on the tensor cores)
+  st = (m > 1 && !c->wops.empty()) ? launch_list(c, c->wkp, false) : launch_list(c, c->kp, true);
   if (st != DEC_OK) return st;
   if (logits_dev && c->cfg.vocab)
     CUDA_TRY(cudaMemcpyAsync(logits_dev, c->ws + c->lay.logits, (size_t)m * c->cfg.vocab * 4, cudaMemcpyDeviceToDevice,

@@ -38,6 +38,7 @@ constexpr int kMaxSlotBytes = 16384;             // one warp's ring slot at most
 constexpr int kSmemLimit = 232448;               // dynamic shared memory per CTA on sm_103a
 constexpr int kNoAllocScratchBytes = 64 * 1024;  // static scratch of the allocation-free LM head
 constexpr int kAttnTcRows = 16;                  // KV rows of one tensor-core attention tile
+constexpr int kGemvTcRows = 16;                  // weight rows of one tensor-core GEMV tile
 constexpr int kAttnTcBoxBytes = kAttnTcRows * 128;  // one 64-column box of a tile (swizzle span 128 B)
 
 enum OpType : int32_t {
@@ -60,7 +61,8 @@ struct OpDesc {
   int32_t K, R, Kc, pair;             // cols, rows per tile, columns per tile, gate/up pair rows
   int32_t ticket, ctr;                // ticket index (LM head argmax); this op's arrival counter
   int32_t wait_ctr, wait_n;           // counter of the op producing this op's input, arrivals / step
-  int32_t aux_ctr, pad0;              // attention: first per-kv-head counter; routed ops: router's
+  int32_t aux_ctr, tc;                // attention: first per-kv-head counter; routed ops: router's;
+                                      // tc: tensor-core tiles (multi-token lists: 16-row boxes by TMA)
   int32_t norm, xsrc;                 // input = RMSNorm(x) * gain; source of x
   int32_t slot0, slot1;               // expert slots [slot0, slot1) (slot1 < 0: up to n_slots)
   int32_t x_idx, unit;                // hidden-stream entry of x (X_F32); row granularity of the CTA split
@@ -86,6 +88,9 @@ struct OpDesc {
                                       // [Mmax][H] (a layer run on its own hands its result back)
   int32_t* topk_idx_out;              // router: also store each token's top-k experts, [m][top_k]
   float* topk_w_out;                  // router: and their routing weights, [m][top_k]
+  const CUtensorMap* tmap;            // tc ops: the weight matrix as a 2D tensor (K columns x N rows),
+                                      // boxes of 64 columns x kGemvTcRows rows, 128-byte swizzle
+  int32_t kw, pad1;                   // column split: columns per warp (0: Kc, in one tile)
 };
 
 struct RouteBlock {
@@ -136,7 +141,8 @@ struct KParams {
   int32_t n_steps, pad2;              // greedy steps this launch runs (> 1: chained in the kernel)
   uint64_t* hs;                       // hidden stream, tagged [2L + 1][Mmax][H]
   uint64_t* trace;                    // DEC_TRACE builds: [n_ctas][n_ops][kTraceFields] %globaltimer stamps
-  int32_t attn_tc, pad3;              // 1: bf16 attention tiles come by TMA tensor copies (128-byte
+  int32_t attn_tc, attn_window;       // attn_window: 0 global, W > 0 the last W positions per token;
+                                      // attn_tc 1: bf16 attention tiles come by TMA tensor copies (128-byte
                                       // swizzle) and run on the tensor cores
   CUtensorMap tmap_k, tmap_v;         // the bf16 key / value caches as 2D tensors: 128 columns x
                                       // (L n_kv cap) rows, boxes of 64 columns x kAttnTcRows rows

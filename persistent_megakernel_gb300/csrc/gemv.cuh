@@ -18,6 +18,44 @@
 #include "dec_internal.h"
 #include "ptx.cuh"
 
+#ifndef DEC_MX_H2
+#define DEC_MX_H2 1  // MXFP4: products and block partial sums in f16x2, one f32 conversion per block
+#endif
+
+namespace decimpl {
+#if DEC_MX_H2
+__device__ __forceinline__ uint32_t e2m1x2_to_h2(uint32_t byte) {
+  uint32_t h;
+  asm("{ .reg .b8 t; .reg .b16 s; cvt.u16.u32 s, %1; cvt.u8.u16 t, s; cvt.rn.f16x2.e2m1x2 %0, t; }" : "=r"(h) : "r"(byte));
+  return h;
+}
+__device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+// (lo, hi) -> f16x2 with lo in the low half
+__device__ __forceinline__ uint32_t f32x2_to_h2(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+__device__ __forceinline__ float2 h2_to_float2(uint32_t h) {
+  float2 r;
+  asm("{ .reg .b16 lo, hi; mov.b32 {lo, hi}, %2; cvt.f32.f16 %0, lo; cvt.f32.f16 %1, hi; }" : "=f"(r.x), "=f"(r.y) : "r"(h));
+  return r;
+}
+// A chunk's activations are scaled by 2^-k, k >= 0 the smallest shift that brings their largest
+// magnitude below 2^8: products with e2m1 weights (|w| <= 6) stay below 1536 and a partial sum
+// of 8 products below 2^14, far inside f16's range. 2^k multiplies the block's fp32 result.
+__device__ __forceinline__ int h2_shift(float amax) {
+  const int e = (int)((__float_as_uint(amax) >> 23) & 0xFFu) - 127;
+  return e > 7 ? min(e - 7, 120) : 0;
+}
+__device__ __forceinline__ float pow2f(int k) { return __uint_as_float((uint32_t)(127 + k) << 23); }
+#endif
+}  // namespace decimpl
+
 namespace decimpl {
 
 template <int WT>
@@ -113,6 +151,69 @@ __device__ __forceinline__ void warp_gemv(const uint8_t* slot, int nr, int kn, i
         w[j] = (j < nr) ? *reinterpret_cast<const uint4*>(slot + (size_t)j * rb + v * 16) : make_uint4(0u, 0u, 0u, 0u);
         X[j] = (j < nr) ? e8m0_to_float(scales[(size_t)j * (kn / 32) + v]) : 0.f;
       }
+#if DEC_MX_H2
+      {
+        // per token: the chunk's activation scale first, then both halves in f16x2
+        int up[MT];
+        uint32_t hs[NR][MT][2];
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+          float amax = 0.f;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float4 x = (MT == 1 || m < Mv) ? *reinterpret_cast<const float4*>(act + m * K + ((q * NVt + vb + v) << 2))
+                                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w))));
+          }
+          up[m] = h2_shift(amax);
+#pragma unroll
+          for (int j = 0; j < NR; ++j) hs[j][m][0] = hs[j][m][1] = 0u;
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t ah[MT][8];
+#pragma unroll
+          for (int m = 0; m < MT; ++m) {
+            const float down = pow2f(-up[m]);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float4 x = (MT == 1 || m < Mv)
+                                   ? *reinterpret_cast<const float4*>(act + m * K + (((4 * h + q) * NVt + vb + v) << 2))
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+              ah[m][2 * q] = f32x2_to_h2(x.x * down, x.y * down);
+              ah[m][2 * q + 1] = f32x2_to_h2(x.z * down, x.w * down);
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < NR; ++j) {
+            const uint32_t w0 = h ? w[j].z : w[j].x, w1 = h ? w[j].w : w[j].y;
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+              uint32_t a0 = hs[j][m][0], a1 = hs[j][m][1];
+              a0 = hfma2_u32(e2m1x2_to_h2(w0 & 0xFFu), ah[m][0], a0);
+              a1 = hfma2_u32(e2m1x2_to_h2((w0 >> 8) & 0xFFu), ah[m][1], a1);
+              a0 = hfma2_u32(e2m1x2_to_h2((w0 >> 16) & 0xFFu), ah[m][2], a0);
+              a1 = hfma2_u32(e2m1x2_to_h2(w0 >> 24), ah[m][3], a1);
+              a0 = hfma2_u32(e2m1x2_to_h2(w1 & 0xFFu), ah[m][4], a0);
+              a1 = hfma2_u32(e2m1x2_to_h2((w1 >> 8) & 0xFFu), ah[m][5], a1);
+              a0 = hfma2_u32(e2m1x2_to_h2((w1 >> 16) & 0xFFu), ah[m][6], a0);
+              a1 = hfma2_u32(e2m1x2_to_h2(w1 >> 24), ah[m][7], a1);
+              hs[j][m][0] = a0;
+              hs[j][m][1] = a1;
+            }
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < NR; ++j)
+#pragma unroll
+          for (int m = 0; m < MT; ++m) {
+            const float2 f0 = h2_to_float2(hs[j][m][0]), f1 = h2_to_float2(hs[j][m][1]);
+            const float Xe = X[j] * pow2f(up[m]);
+            A.c[j][m][0] = ffma2(make_float2(Xe, Xe), make_float2(f0.x + f1.x, f0.y + f1.y), A.c[j][m][0]);
+          }
+        continue;
+      }
+#endif
       float2 blk[NR][MT];
 #pragma unroll
       for (int j = 0; j < NR; ++j)
@@ -195,17 +296,51 @@ struct ActRegs {
   float4 a[NI][WCfg<WT>::Q];
 };
 
+#if DEC_MX_H2
+// MXFP4: f16 pairs (elements 2k, 2k+1 of chunk i in h[i][k]) scaled by 2^-k_i; e[i] = 2^k_i.
+template <int NI>
+struct ActRegs<W_MXFP4, NI> {
+  uint32_t h[NI][16];
+  float e[NI];
+};
+#endif
+
 // Load chunks v = lane + 32 i (i < NI) of columns [c0, c0 + cn) of the op's activation plane.
 template <int WT, int NI>
 __device__ __forceinline__ void act_regs_load(ActRegs<WT, NI>& R, const float* act, int K, int c0, int cn, int lane) {
   constexpr int CW = WCfg<WT>::CW, Q = WCfg<WT>::Q;
   const int NVt = K / CW, vb = c0 / CW, NV = cn / CW;
+#if DEC_MX_H2
+  if constexpr (WT == W_MXFP4) {
 #pragma unroll
-  for (int i = 0; i < NI; ++i) {
-    const int v = lane + 32 * i;
+    for (int i = 0; i < NI; ++i) {
+      const int v = lane + 32 * i;
+      float4 x[8];
+      float amax = 0.f;
 #pragma unroll
-    for (int q = 0; q < Q; ++q)
-      R.a[i][q] = v < NV ? *reinterpret_cast<const float4*>(act + ((q * NVt + vb + v) << 2)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int q = 0; q < 8; ++q) {
+        x[q] = v < NV ? *reinterpret_cast<const float4*>(act + ((q * NVt + vb + v) << 2)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(x[q].x), fabsf(x[q].y)), fmaxf(fabsf(x[q].z), fabsf(x[q].w))));
+      }
+      const int k = h2_shift(amax);
+      const float down = pow2f(-k);
+      R.e[i] = pow2f(k);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        R.h[i][2 * q] = f32x2_to_h2(x[q].x * down, x[q].y * down);
+        R.h[i][2 * q + 1] = f32x2_to_h2(x[q].z * down, x[q].w * down);
+      }
+    }
+  } else
+#endif
+  {
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+      const int v = lane + 32 * i;
+#pragma unroll
+      for (int q = 0; q < Q; ++q)
+        R.a[i][q] = v < NV ? *reinterpret_cast<const float4*>(act + ((q * NVt + vb + v) << 2)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
   }
 }
 
@@ -283,6 +418,23 @@ __device__ __forceinline__ void warp_gemv_reg(const uint8_t* slot, int nr, int k
       } else {
         const int v = lane + 32 * i;
         const bool ok = v < NV;
+#if DEC_MX_H2
+#pragma unroll
+        for (int j = 0; j < NR; ++j) {
+          const uint32_t ww[4] = {wg[j].x, wg[j].y, wg[j].z, wg[j].w};
+          uint32_t h0 = 0u, h1 = 0u;  // two f16x2 partial sums of 8 products each
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            h0 = hfma2_u32(e2m1x2_to_h2(ww[q] & 0xFFu), R.h[i][4 * q], h0);
+            h1 = hfma2_u32(e2m1x2_to_h2((ww[q] >> 8) & 0xFFu), R.h[i][4 * q + 1], h1);
+            h0 = hfma2_u32(e2m1x2_to_h2((ww[q] >> 16) & 0xFFu), R.h[i][4 * q + 2], h0);
+            h1 = hfma2_u32(e2m1x2_to_h2(ww[q] >> 24), R.h[i][4 * q + 3], h1);
+          }
+          const float2 f0 = h2_to_float2(h0), f1 = h2_to_float2(h1);
+          const float X = (ok && j < nr) ? e8m0_to_float(scales[(size_t)j * (kn / 32) + v]) * R.e[i] : 0.f;
+          A.c[j][0][0] = ffma2(make_float2(X, X), make_float2(f0.x + f1.x, f0.y + f1.y), A.c[j][0][0]);
+        }
+#else
 #pragma unroll
         for (int j = 0; j < NR; ++j) {
           const uint32_t ww[4] = {wg[j].x, wg[j].y, wg[j].z, wg[j].w};
@@ -301,6 +453,7 @@ __device__ __forceinline__ void warp_gemv_reg(const uint8_t* slot, int nr, int k
           A.c[j][0][0] = ffma2(xx, b0, A.c[j][0][0]);
           A.c[j][0][1] = ffma2(xx, b1, A.c[j][0][1]);
         }
+#endif
       }
     }
     acc_pin(A);

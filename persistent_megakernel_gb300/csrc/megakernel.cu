@@ -233,11 +233,17 @@ __device__ __forceinline__ void warp_rows(int a, int b, int unit, int w, int& aw
 }
 
 // Attention: every kv head has ns splits of the positions [0, S), S = pos + M.
-__device__ __forceinline__ void split_range(int S, int ns, int j, int& head, int& s, int& p0, int& p1) {
+__device__ __forceinline__ void split_range(int lo, int S, int ns, int j, int& head, int& s, int& p0, int& p1) {
   head = j / ns;
   s = j % ns;
-  p0 = (int)((long long)S * s / ns);
-  p1 = (int)((long long)S * (s + 1) / ns);
+  p0 = lo + (int)((long long)(S - lo) * s / ns);
+  p1 = lo + (int)((long long)(S - lo) * (s + 1) / ns);
+}
+
+// First cached position a call's attention reads: with a sliding window of W positions the
+// call's first token (at pos) sees pos - W + 1 .. pos; 0 for global attention.
+__device__ __forceinline__ int attn_lo(const KParams& p, int pos) {
+  return p.attn_window > 0 ? max(0, pos - p.attn_window + 1) : 0;
 }
 
 // Warps serving token m of an M-token window: m, m + M, ...; this warp is number gi of ng.
@@ -256,6 +262,26 @@ __device__ __forceinline__ int attn_rows(const KParams& p, int slot_bytes) {
 
 __device__ __forceinline__ int row_bytes(int wtype, int K) {
   return wtype == W_BF16 ? 2 * K : (wtype == W_FP8 ? K : K / 2);
+}
+
+// Token m's activations k .. k+3 (k a multiple of 4) as the B operand of the tensor-core GEMV
+// (m16n8k16, eight columns): 16-column step k / 16, lane 4 g + t holds columns g = m (bf16 high
+// parts) and g = m + 4 (the residues), rows 2t, 2t+1 in its first register, 2t+8, 2t+9 in its
+// second. 256 bytes per step: the same bytes as kMmax tokens of fp32.
+__device__ __forceinline__ void put_bfrag(float* act, int m, int k, float4 x) {
+  uint32_t* bf = reinterpret_cast<uint32_t*>(act);
+  const int kk = k >> 4, c = k & 15, reg = c >> 3, t0 = (c & 7) >> 1;
+  const float v[4] = {x.x, x.y, x.z, x.w};
+  float hi[4], lo[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    hi[e] = __bfloat162float(__float2bfloat16_rn(v[e]));
+    lo[e] = v[e] - hi[e];
+  }
+  bf[((kk * 32 + 4 * m + t0) << 1) + reg] = pack_bf16x2(hi[0], hi[1]);
+  bf[((kk * 32 + 4 * m + t0 + 1) << 1) + reg] = pack_bf16x2(hi[2], hi[3]);
+  bf[((kk * 32 + 4 * (m + 4) + t0) << 1) + reg] = pack_bf16x2(lo[0], lo[1]);
+  bf[((kk * 32 + 4 * (m + 4) + t0 + 1) << 1) + reg] = pack_bf16x2(lo[2], lo[3]);
 }
 
 struct Tile {
@@ -313,8 +339,9 @@ struct GemvIter {
     } else if (mode == 3) {
       aw = a;
       bw = b;
-      kw0 = min(K, w * Kc);
-      kw1 = w == kConsumerWarps - 1 ? K : min(K, kw0 + Kc);
+      const int kwid = op.kw ? op.kw : Kc;  // this warp's columns, walked in tiles of Kc
+      kw0 = min(K, w * kwid);
+      kw1 = w == kConsumerWarps - 1 ? K : min(K, kw0 + kwid);
     } else {
       warp_rows(a, b, op.unit, w, aw, bw);
       kw0 = kw1 = 0;
@@ -344,10 +371,14 @@ struct GemvIter {
       t.sl = 0;
       t.r0 = r;
       t.nr = min(R, bw - r);
-      t.kc = kw0;
-      t.kn = kw1 - kw0;
-      t.last_k = true;
-      r += t.nr;
+      t.kc = kw0 + kc;
+      t.kn = min(Kc, kw1 - t.kc);
+      t.last_k = t.kc + t.kn >= kw1;
+      kc += t.kn;
+      if (t.last_k) {
+        kc = 0;
+        r += t.nr;
+      }
       return true;
     }
     if (mode == 2) {
@@ -391,6 +422,7 @@ struct GemvIter {
 // split the warps of token m share the cached positions [p0, min(p1, pos)).
 struct AttnIter {
   int C, S, ns, nsplit, pos, P;
+  int lo;  // first position any token of the call attends to (a sliding window's start)
   int gi, ng;
   int j, q, qe, head;
   bool fresh;
@@ -399,6 +431,7 @@ struct AttnIter {
     C = p.n_ctas;
     pos = pos_;
     S = pos + M;
+    lo = attn_lo(p, pos);
     ns = p.ns_max;
     nsplit = p.n_kv * ns;
     P = P_;
@@ -410,7 +443,7 @@ struct AttnIter {
 
   __device__ __forceinline__ void enter_split() {
     int s, p0, p1;
-    split_range(S, ns, j, head, s, p0, p1);
+    split_range(lo, S, ns, j, head, s, p0, p1);
     const int ce = max(p0, min(p1, pos));
     q = p0 + (int)((long long)(ce - p0) * gi / ng);
     qe = p0 + (int)((long long)(ce - p0) * (gi + 1) / ng);
@@ -492,6 +525,16 @@ struct Producer {
   }
 
   __device__ __forceinline__ void copy_gemv(const OpDesc* op, const Tile& t, uint8_t* dst, uint32_t fb) {
+    if (__ldg(&op->tc)) {
+      // tensor-core tile: boxes of kGemvTcRows rows x 64 columns, 128-byte swizzle, always whole
+      // (rows past the tile are the next rows of the matrix, or zeros past its end; unused)
+      const int nb = t.kn / 64;
+      const CUtensorMap* tm = op->tmap;
+      mbar_expect_tx(fb, (uint32_t)(nb * kGemvTcRows * 128));
+      const uint32_t d = smem_addr(dst);
+      for (int b = 0; b < nb; ++b) tma_load_2d(d + b * kGemvTcRows * 128, tm, t.kc + 64 * b, t.r0, fb, policy);
+      return;
+    }
     const int wtype = __ldg(&op->wtype), K = __ldg(&op->K);
     const int rb = row_bytes(wtype, K);
     const char* base = static_cast<const char*>(op->w) + (size_t)t.mat * __ldg(&op->w_mstride);
@@ -790,11 +833,12 @@ __device__ __forceinline__ float e4m3_to_float_bits(uint32_t x) {
 // One tile of n rows (keys at kr, values at vr; 256 B per bf16 row, 128 B per e4m3 row) for the
 // G_ heads of token m. e4m3 rows hold the codes: the caller folds the keys' scale into q and
 // applies the values' scale to the outputs.
-// vis_base < 0: all rows visible; else row j is this call's row vis_base + j, visible iff <= m.
+// vis_base < 0: cached rows, row j at position row0 + j, visible iff >= lo_m (a sliding window's
+// start for token m); else row j is this call's row vis_base + j, visible iff <= m.
 template <int G_, bool KV8>
 __device__ __forceinline__ void attn_warp_tile(AttnState<G_>& A, const float (&q)[G_][16], const uint8_t* kr,
                                                const uint8_t* vr, int n, int vis_base, int m, float* sc, int P,
-                                               int lane) {
+                                               int lane, int row0 = 0, int lo_m = 0) {
   constexpr int RB = KV8 ? 128 : 256;
   const int grp = lane >> 3, sub = lane & 7;
   // scores: eight lanes per row, 16 dims each, four rows per step
@@ -832,7 +876,7 @@ __device__ __forceinline__ void attn_warp_tile(AttnState<G_>& A, const float (&q
       sv += __shfl_xor_sync(0xffffffffu, sv, 2);
       sv += __shfl_xor_sync(0xffffffffu, sv, 1);
       if (sub == 0 && j < n) {
-        const bool vis = vis_base < 0 || vis_base + j <= m;
+        const bool vis = vis_base < 0 ? row0 + j >= lo_m : vis_base + j <= m;
         sc[h * P + j] = vis ? sv : -INFINITY;
       }
     }
@@ -897,6 +941,8 @@ template <int WT, int MT, int NR, int NI>
 __device__ __noinline__ bool gemv_csplit_entry(const KParams& p, int oi, const OpDesc& op, int M, int a, float* parts);
 template <int MT, int NR, int NI>
 __device__ __noinline__ bool gemv_xsplit_entry(const KParams& p, int oi, const OpDesc& op, int M, int a, float* parts);
+__device__ __noinline__ bool gemv_tc_entry(const KParams& p, int oi, const OpDesc& op, int M, float* xres, int a,
+                                          float* parts);
 template <int MT>
 __device__ __noinline__ bool gemv_slot_entry(const KParams& p, int oi, const OpDesc& op, int sl, int M, int a,
                                              float* accd);
@@ -909,7 +955,7 @@ __device__ __noinline__ bool copy_act_entry(const KParams& p, int oi, float* dst
 template <int G_>
 __device__ __noinline__ bool attn_entry(const KParams& p, int oi, int pos, int M);
 template <int G_>
-__device__ __noinline__ bool attn_tc_entry(const KParams& p, int oi, int r0, int r1, int m_tok, int M);
+__device__ __noinline__ bool attn_tc_entry(const KParams& p, int oi, int r0, int r1, int m_tok, int M, int lo_m);
 
 // A consumer thread's view of the kernel. Built from scratch wherever it is needed (see
 // smem_raw), so out-of-line functions keep it in registers; the ring position of the thread's
@@ -1135,7 +1181,10 @@ struct Consumer {
         x.z *= bf16_lo(g.y);
         x.w *= bf16_hi(g.y);
       }
-      *reinterpret_cast<float4*>(s.act + m * H + act_pos(4 * k4, cw, nvt)) = x;
+      if (op.tc)
+        put_bfrag(s.act, m, 4 * k4, x);
+      else
+        *reinterpret_cast<float4*>(s.act + m * H + act_pos(4 * k4, cw, nvt)) = x;
     };
     bool ok = true;
     if (op.xsrc == X_F32) {
@@ -1172,12 +1221,15 @@ struct Consumer {
   // dst = M rows of K tagged words polled from global (row stride src_stride words), in the
   // quarter-plane layout of chunk width cw.
   __device__ __forceinline__ bool copy_act(float* dst, const uint64_t* src, int M, int K, int src_stride, int cw, int oi) {
-    const int K4 = K / 4, nvt = K / cw;
+    const int K4 = K / 4, nvt = cw ? K / cw : 0;
     return gather<kCopyU, 4>(
         M * K4, [&](int i) { return src + (size_t)(i / K4) * src_stride + 4 * (i % K4); },
         [&](int i, const float (&v)[4]) {
-          *reinterpret_cast<float4*>(dst + (i / K4) * K + act_pos(4 * (i % K4), cw, nvt)) =
-              make_float4(v[0], v[1], v[2], v[3]);
+          if (cw == 0)  // the tensor-core B operand layout
+            put_bfrag(dst, i / K4, 4 * (i % K4), make_float4(v[0], v[1], v[2], v[3]));
+          else
+            *reinterpret_cast<float4*>(dst + (i / K4) * K + act_pos(4 * (i % K4), cw, nvt)) =
+                make_float4(v[0], v[1], v[2], v[3]);
         },
         oi, 9);
   }
@@ -1490,11 +1542,109 @@ struct Consumer {
     return true;
   }
 
+  // Tensor-core tiles of a multi-token call (bf16 matrices of the multi-token list): every tile is
+  // kGemvTcRows weight rows x Kc columns in boxes of 64 columns (128-byte swizzle); per 16-column
+  // step one ldmatrix gives the A fragments (weights) and the B fragments (the tokens' bf16 high
+  // parts in columns 0-3 and residues in 4-7, staged by the prologue) come from shared memory;
+  // one m16n8k16 MMA with fp32 accumulation. A row group's results are D[row][m] + D[row][m + 4],
+  // handed to the same per-(row, token) outputs as the CUDA-core path, eight rows at a time.
+  __device__ __forceinline__ bool gemv_tc_t(int oi, const OpDesc& op, int M, float* xres, int a, float* parts) {
+    constexpr int MT = kMmax;
+    GemvIter it;
+    it.init(op, p.n_ctas, blockIdx.x, warp, 0, nullptr, 0);
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    float best_v = -INFINITY;
+    int best_i = 0x7FFFFFFF;
+    const uint32_t* bf = reinterpret_cast<const uint32_t*>(s.act);
+    const int mq = lane >> 3, rr = lane & 7;
+    const uint32_t aoff = (uint32_t)(((mq & 1) * 8 + rr) * 128);  // A: matrices 1, 3 = rows 8-15
+    const int i = lane >> 2, m = lane & 3;                          // result lane: row i of 8, token m
+    // norm ops: the RMSNorm scale applies to row sums (a column split adds it in the epilogue)
+    const float rs = (op.norm && !op.csplit) ? rstd(m < M ? m : 0) : 1.f;
+    Tile t;
+    bool ok = true;
+    if (op.csplit && it.kw0 >= it.kw1)  // a warp without columns contributes zeros
+      for (int k = lane; k < (it.bw - it.aw) * M; k += 32) parts[warp * (it.bw - it.aw) * M + k] = 0.f;
+    while (it.next(t)) {
+      uint8_t* slot;
+      uint32_t eb;
+      if (!next_slot(oi, slot, eb)) {
+        ok = false;
+        break;
+      }
+      const uint32_t sb = smem_addr(slot);
+      const int ns = t.kn >> 4, kg0 = t.kc >> 4;
+#pragma unroll 4
+      for (int j = 0; j < ns; ++j) {
+        const int c = ((j & 3) << 1) + (mq >> 1);  // 16-byte column chunk within the 64-column box
+        uint32_t af[4];
+        ldsm_x4(sb + (uint32_t)((j >> 2) * kGemvTcRows * 128) + aoff + (uint32_t)((c ^ rr) << 4), af);
+        const uint2 b = *reinterpret_cast<const uint2*>(bf + ((kg0 + j) * 32 + lane) * 2);
+        mma_bf16_16816(d, af, b.x, b.y);
+      }
+      release(eb);
+      if (!t.last_k) continue;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int src = 4 * i + (m >> 1);
+        const float x0 = __shfl_sync(0xffffffffu, half ? d[2] : d[0], src);
+        const float x1 = __shfl_sync(0xffffffffu, half ? d[3] : d[1], src);
+        const float y0 = __shfl_sync(0xffffffffu, half ? d[2] : d[0], src + 2);
+        const float y1 = __shfl_sync(0xffffffffu, half ? d[3] : d[1], src + 2);
+        const float v = ((m & 1) ? x1 + y1 : x0 + y0) * rs;
+        const int r0 = t.r0 + 8 * half, nr = min(8, t.nr - 8 * half);
+        if (nr <= 0) break;
+        const bool mine = lane < nr * MT && m < M;
+        if (op.csplit) {  // column split: this warp's partial sums, added across warps afterwards
+          if (mine) parts[(warp * (it.bw - it.aw) + (r0 + i - a)) * M + m] = v;
+          continue;
+        }
+        switch (op.type) {
+          case OP_QKV:
+          case OP_ROUTER:
+            if (mine) st_tagged(op.out + (size_t)m * op.N + r0 + i, v, tag);
+            break;
+          case OP_OPROJ:
+          case OP_DOWN:
+            if (mine) put_x(op, m, r0 + i, xres[(r0 + i - a) * M + m] + v);
+            break;
+          case OP_GATEUP: {
+            const float g = __shfl_sync(0xffffffffu, v, ((2 * i) * MT + m) & 31);
+            const float u = __shfl_sync(0xffffffffu, v, ((2 * i + 1) * MT + m) & 31);
+            if (lane < (nr / 2) * MT && m < M) st_tagged(op.out + (size_t)m * (op.N / 2) + r0 / 2 + i, silu(g) * u, tag);
+            break;
+          }
+          case OP_LMHEAD:
+            if (mine) {
+              const int row = r0 + i;
+              op.logits[(size_t)m * op.N + row] = v;
+              if (v > best_v || (v == best_v && row < best_i)) {
+                best_v = v;
+                best_i = row;
+              }
+            }
+            break;
+          default:
+            break;
+        }
+      }
+      d[0] = d[1] = d[2] = d[3] = 0.f;
+    }
+    if (op.type == OP_LMHEAD) {
+      // lane l tracked token l % 4, as on the CUDA-core path
+      s.resw[warp * 64 + lane] = best_v;
+      reinterpret_cast<int*>(s.resw)[warp * 64 + 32 + lane] = best_i;
+    }
+    return ok;
+  }
+
   // Instantiations: tile rows NR (bf16 2/4/8, FP8 4/8, MXFP4 8; the host's R fits) and, for
   // one token, the register chunks NI the warp's columns need (0: activations stay in shared
   // memory). The host only makes column-split ops whose columns fit in registers.
   template <int MT>
   __device__ bool gemv_dispatch(int oi, const OpDesc& op, int M, float* xres, int a, float* accd) {
+    if constexpr (MT == kMmax)
+      if (op.tc) return gemv_tc_entry(p, oi, op, M, xres, a, accd);
     const int kw = op.csplit ? op.Kc : op.K;  // columns one warp multiplies
     const bool whole = op.csplit || (op.Kc == op.K && op.type != OP_EXP_DOWN);
     if (op.wtype == W_BF16) {
@@ -1580,7 +1730,7 @@ struct Consumer {
       case OP_OPROJ:
       case OP_DOWN:
         cta_rows(op.N, op.unit, p.n_ctas, blockIdx.x, g.a, g.b);
-        g.xres = s.act + M * op.K;
+        g.xres = s.act + (op.tc ? kMmax : M) * op.K;  // tensor-core B operand: kMmax tokens' bytes
         if (op.csplit) g.accd = g.xres + (g.b - g.a) * M;  // per-warp partial sums
         break;
       case OP_EXP_DOWN: {
@@ -1593,7 +1743,7 @@ struct Consumer {
       default:
         if (op.csplit) {
           cta_rows(op.N, op.unit, p.n_ctas, blockIdx.x, g.a, g.b);
-          g.accd = s.act + M * op.K;  // per-warp partial sums
+          g.accd = s.act + (op.tc ? kMmax : M) * op.K;  // per-warp partial sums
         }
         break;
     }
@@ -1615,7 +1765,7 @@ struct Consumer {
     switch (op.type) {
       case OP_OPROJ:
       case OP_DOWN:
-        ok &= copy_act(s.act, op.act, M, op.K, op.K, cw, oi);
+        ok &= copy_act(s.act, op.act, M, op.K, op.K, op.tc ? 0 : cw, oi);
         if (tid == 0) TRACE(p, oi, 8, gtimer());
         ok &= load_residual(op, g.xres, g.a, g.b, M, oi);
         break;
@@ -1691,34 +1841,94 @@ struct Consumer {
   __device__ __forceinline__ void lmhead_finish(const OpDesc& op, int M) {
     consumer_sync();
     const int MT = M == 1 ? 1 : 4;  // lane l of a warp tracked token l % MT
+    {
+      // this CTA's best per token: the lanes of each warp that tracked the same token, by
+      // shuffles; then the warps' bests (lowest index among equal logits throughout)
+      float v = s.resw[warp * 64 + lane];
+      int i = reinterpret_cast<const int*>(s.resw)[warp * 64 + 32 + lane];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, i, o);
+        if (o >= MT && (ov > v || (ov == v && oi < i))) {
+          v = ov;
+          i = oi;
+        }
+      }
+      if (lane < MT) {
+        s.red[lane * 8 + warp] = v;
+        reinterpret_cast<int*>(s.red)[32 + lane * 8 + warp] = i;
+      }
+    }
+    consumer_sync();
     if (tid < M) {
       float v = -INFINITY;
       int i = 0x7FFFFFFF;
-      for (int w = 0; w < kConsumerWarps; ++w)
-        for (int l = tid; l < 32; l += MT) {
-          const float wv = s.resw[w * 64 + l];
-          const int wi = reinterpret_cast<const int*>(s.resw)[w * 64 + 32 + l];
-          if (wv > v || (wv == v && wi < i)) {
-            v = wv;
-            i = wi;
-          }
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        const float wv = s.red[tid * 8 + w];
+        const int wi = reinterpret_cast<const int*>(s.red)[32 + tid * 8 + w];
+        if (wv > v || (wv == v && wi < i)) {
+          v = wv;
+          i = wi;
         }
+      }
       p.am_val[blockIdx.x * kMmax + tid] = v;
       p.am_idx[blockIdx.x * kMmax + tid] = i;
     }
     if (ticket(op.ticket, p.n_ctas)) {
-      if (tid < M) {
-        float v = -INFINITY;
-        int i = 0x7FFFFFFF;
-        for (int c = 0; c < p.n_ctas; ++c) {
-          const float cv = __ldcg(p.am_val + c * kMmax + tid);
-          const int ci = __ldcg(p.am_idx + c * kMmax + tid);
-          if (cv > v || (cv == v && ci < i)) {
-            v = cv;
-            i = ci;
+      // the last CTA reduces every CTA's best in parallel: each thread loads the partials of its
+      // CTAs (all tokens' loads in flight together), then warps, then the warps' bests
+      float v[kMmax];
+      int ix[kMmax];
+#pragma unroll
+      for (int m = 0; m < kMmax; ++m) {
+        v[m] = -INFINITY;
+        ix[m] = 0x7FFFFFFF;
+      }
+      for (int c = tid; c < p.n_ctas; c += kConsumerThreads) {
+        float cv[kMmax];
+        int ci[kMmax];
+#pragma unroll
+        for (int m = 0; m < kMmax; ++m) {
+          cv[m] = m < M ? __ldcg(p.am_val + c * kMmax + m) : -INFINITY;
+          ci[m] = m < M ? __ldcg(p.am_idx + c * kMmax + m) : 0x7FFFFFFF;
+        }
+#pragma unroll
+        for (int m = 0; m < kMmax; ++m)
+          if (cv[m] > v[m] || (cv[m] == v[m] && ci[m] < ix[m])) {
+            v[m] = cv[m];
+            ix[m] = ci[m];
+          }
+      }
+#pragma unroll
+      for (int m = 0; m < kMmax; ++m) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, v[m], o);
+          const int oi = __shfl_xor_sync(0xffffffffu, ix[m], o);
+          if (ov > v[m] || (ov == v[m] && oi < ix[m])) {
+            v[m] = ov;
+            ix[m] = oi;
           }
         }
-        p.am_out[tid] = i < p.V ? i : 0;  // no ordered logit (NaN inputs): a valid token, never a wild one
+        if (lane == 0) {
+          s.red[m * 8 + warp] = v[m];
+          s.resw[m * 8 + warp] = __int_as_float(ix[m]);
+        }
+      }
+      consumer_sync();
+      if (tid < M) {
+        float bv = -INFINITY;
+        int bi = 0x7FFFFFFF;
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          const float wv = s.red[tid * 8 + w];
+          const int wi = __float_as_int(s.resw[tid * 8 + w]);
+          if (wv > bv || (wv == bv && wi < bi)) {
+            bv = wv;
+            bi = wi;
+          }
+        }
+        p.am_out[tid] = bi < p.V ? bi : 0;  // no ordered logit (NaN inputs): a valid token, never a wild one
       }
     }
   }
@@ -1732,7 +1942,7 @@ struct Consumer {
   // keep about 16 bits of mantissa and the two rows' products add up in fp32. Online softmax in
   // base 2 on the score fragments; the state (max, sum, output) goes to the warp's merge slice.
   template <int G_>
-  __device__ __forceinline__ bool attn_tc_t(int oi, int r0, int r1, int m_tok, int M) {
+  __device__ __forceinline__ bool attn_tc_t(int oi, int r0, int r1, int m_tok, int M, int lo_m) {
     static_assert(G_ <= 8, "at most 8 query heads per kv head on the tensor-core path");
     const int P = kAttnTcRows;
     const AttnScratch a = attn_scratch(p, s, M, P);
@@ -1792,7 +2002,7 @@ struct Consumer {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int row = 8 * j + 2 * tq + e;
-          sv[j][e] = row < nr ? sc4[j][e] + sc4[j][2 + e] : -INFINITY;
+          sv[j][e] = (row < nr && r + row >= lo_m) ? sc4[j][e] + sc4[j][2 + e] : -INFINITY;
           mx = fmaxf(mx, sv[j][e]);
         }
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
@@ -1885,6 +2095,8 @@ struct Consumer {
     const float qscale = 1.4426950408889634f / sqrtf(128.f);  // log2(e) / sqrt(d)
     int m_tok, gi, ng;
     token_group(warp, M, m_tok, gi, ng);
+    // this warp's token (at pos + m_tok) sees cached positions from lo_m on
+    const int lo_m = p.attn_window > 0 ? max(0, pos + m_tok - p.attn_window + 1) : 0;
     AttnIter it;
     it.init(p, blockIdx.x, warp, pos, M, P);
     float* sc = a.sc + warp * G * P;
@@ -1894,7 +2106,7 @@ struct Consumer {
     const int GR = (G + 2) * 32;  // float4 groups of one token's q, k, v rows of the kv group
     for (; it.j < it.nsplit; it.next_split()) {
       int head, sidx, p0, p1;
-      split_range(it.S, ns, it.j, head, sidx, p0, p1);
+      split_range(it.lo, it.S, ns, it.j, head, sidx, p0, p1);
       const int nb = max(p0, pos), nn = max(0, p1 - nb);  // this call's own rows in the split
       // CTA prologue: poll the group's q (and, for the split holding this call's rows, k and v)
       // in one batch; rotate and scale the queries; round, keep and append the own rows
@@ -1991,7 +2203,7 @@ struct Consumer {
         // through its slice of the merge scratch
         if (it.fresh) it.enter_split();
         save_tiles();
-        if (!attn_tc_entry<G_>(p, oi, it.q, it.qe, m_tok, M)) ok = false;
+        if (!attn_tc_entry<G_>(p, oi, it.q, it.qe, m_tok, M, lo_m)) ok = false;
         n_tiles = s.ntiles[warp];
         it.q = it.qe;
         load_q();  // for this call's own rows, after the call (nothing to keep live across it)
@@ -2014,9 +2226,9 @@ struct Consumer {
             break;
           }
           if (p.kv_fp8)
-            attn_warp_tile<G_, true>(A, q, slot, slot + t.nr * rb, t.nr, -1, m_tok, sc, P, lane);
+            attn_warp_tile<G_, true>(A, q, slot, slot + t.nr * rb, t.nr, -1, m_tok, sc, P, lane, t.r0, lo_m);
           else
-            attn_warp_tile<G_, false>(A, q, slot, slot + t.nr * rb, t.nr, -1, m_tok, sc, P, lane);
+            attn_warp_tile<G_, false>(A, q, slot, slot + t.nr * rb, t.nr, -1, m_tok, sc, P, lane, t.r0, lo_m);
           release(eb);
         }
       }
@@ -2073,7 +2285,7 @@ struct Consumer {
     it2.init(p, blockIdx.x, warp, pos, M, P);
     for (; it2.j < it2.nsplit; it2.next_split()) {
       int head, sidx, p0, p1;
-      split_range(it2.S, ns, it2.j, head, sidx, p0, p1);
+      split_range(it2.lo, it2.S, ns, it2.j, head, sidx, p0, p1);
       const uint64_t* hp = lpart + (size_t)(head * ns) * sstride;
       const int total = MG * 32;  // float4 outputs of this kv head
       const int o0 = (int)((long long)total * sidx / ns), o1 = (int)((long long)total * (sidx + 1) / ns);
@@ -2221,6 +2433,14 @@ __device__ __noinline__ bool gemv_csplit_entry(const KParams& p, int oi, const O
   return ok;
 }
 
+__device__ __noinline__ bool gemv_tc_entry(const KParams& p, int oi, const OpDesc& op, int M, float* xres, int a,
+                                          float* parts) {
+  Consumer c(p);
+  const bool ok = c.gemv_tc_t(oi, op, M, xres, a, parts);
+  c.save_tiles();
+  return ok;
+}
+
 template <int MT, int NR, int NI>
 __device__ __noinline__ bool gemv_xsplit_entry(const KParams& p, int oi, const OpDesc& op, int M, int a, float* parts) {
   Consumer c(p);
@@ -2273,9 +2493,9 @@ __device__ __noinline__ bool attn_entry(const KParams& p, int oi, int pos, int M
 }
 
 template <int G_>
-__device__ __noinline__ bool attn_tc_entry(const KParams& p, int oi, int r0, int r1, int m_tok, int M) {
+__device__ __noinline__ bool attn_tc_entry(const KParams& p, int oi, int r0, int r1, int m_tok, int M, int lo_m) {
   Consumer c(p);
-  const bool ok = c.attn_tc_t<G_>(oi, r0, r1, m_tok, M);
+  const bool ok = c.attn_tc_t<G_>(oi, r0, r1, m_tok, M, lo_m);
   c.save_tiles();
   return ok;
 }

@@ -42,6 +42,7 @@ def make_config(shape, capacity: int, max_verify: int = 1, mode: str = "persiste
     c.mode = _MODE[mode]
     c.spin_timeout_ns = timeout_ns
     c.num_ctas = num_ctas
+    c.attn_window = getattr(shape, "attn_window", 0)
     c.kv_dtype = B.DEC_FP8_E4M3 if getattr(shape, "kv_dtype", "bf16") == "fp8" else B.DEC_BF16
     return c
 

@@ -64,12 +64,15 @@ def head_bytes(s) -> int:
 
 
 def kv_bytes(s, pos: int, m: int = 1) -> int:
-    """KV bytes one step reads: keys and values of positions [0, pos + m) of every layer
-    (the window's own new rows included), bf16 (2 B) or FP8 e4m3 (1 B) per element."""
+    """KV bytes one step reads: keys and values of positions [lo, pos + m) of every layer
+    (the window's own new rows included; lo = 0, or pos - W + 1 with a sliding window of W
+    positions), bf16 (2 B) or FP8 e4m3 (1 B) per element."""
     if not s.attn:
         return 0
     eb = 1 if getattr(s, "kv_dtype", "bf16") == "fp8" else 2
-    return s.n_layers * 2 * s.n_kv * s.head_dim * eb * (pos + m)
+    w = getattr(s, "attn_window", 0)
+    lo = max(0, pos - w + 1) if w > 0 else 0
+    return s.n_layers * 2 * s.n_kv * s.head_dim * eb * (pos + m - lo)
 
 
 def algorithmic_bytes(s, pos: int, m: int = 1, n_routed_active: int | None = None) -> int:

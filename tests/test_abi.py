@@ -38,11 +38,20 @@ def test_exports_every_declared_symbol(B):
     assert sorted(B.EXPORTS) == names
 
 
-def test_struct_layouts_match_header(B):
-    # dec_config: 15 ints, 2 floats, 3 enums, a uint64 (8-aligned), an int -> 96 bytes
-    assert ctypes.sizeof(B.DecConfig) == 96
-    assert B.DecConfig.spin_timeout_ns.offset == 80
-    assert ctypes.sizeof(B.DecTensor) == 40 and B.DecTensor.values.offset == 24
+def test_struct_layouts_match_header(B, tmp_path):
+    # the binding's structs against the header, measured by a host compile of include/dec.h
+    import subprocess
+    src = tmp_path / "cfg.c"
+    src.write_text(
+        '#include <stddef.h>\n#include <stdio.h>\n#include "dec.h"\n'
+        'int main(void) { printf("%zu %zu %zu %zu %zu %zu\\n", sizeof(dec_config), '
+        'offsetof(dec_config, spin_timeout_ns), offsetof(dec_config, kv_dtype), offsetof(dec_config, attn_window), '
+        'sizeof(dec_tensor), offsetof(dec_tensor, values)); return 0; }\n')
+    exe = tmp_path / "cfg"
+    subprocess.check_call(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)])
+    got = [int(x) for x in subprocess.check_output([str(exe)]).split()]
+    assert got == [ctypes.sizeof(B.DecConfig), B.DecConfig.spin_timeout_ns.offset, B.DecConfig.kv_dtype.offset,
+                   B.DecConfig.attn_window.offset, ctypes.sizeof(B.DecTensor), B.DecTensor.values.offset]
 
 
 def test_routing_block_layout_matches_reader(tmp_path):
