@@ -323,11 +323,12 @@ def timed_generate(dec, ctx_handle, tok0, pos0, K, launches_per_step, chain=CHAI
 
 def run_verify(args, rank, ws, local):
     """Verify windows of k tokens (the MTP verify step of the Ling-3.0-flash DGX Spark article,
-    "optimisation 3"): each call feeds the model's last prediction plus k-1 seeded draft tokens at
-    the next k positions, one window after another (positions advance by k, as if every draft
-    were accepted), and reads back the k argmaxes and the accepted count, so the host waits for
-    every window. value = window tokens per second; roofline = the window's algorithmic bytes
-    (weights once, the union of the window's experts, the KV rows read) over its time."""
+    "optimisation 3"): each call feeds k tokens at the next k positions (positions advance by k,
+    as if every draft were accepted). value: windows launched back to back with no readback,
+    CUDA events on the library's stream; e2e: the same windows through dec_verify with the
+    model's last prediction fed back as each window's first token and the k argmaxes and the
+    accepted count read back every window. roofline = the window's algorithmic bytes (weights
+    once, the union of the window's experts, the KV rows read) over its device time."""
     import torch
     import synth
     from persistent_megakernel_gb300 import build as pbuild
@@ -349,23 +350,34 @@ def run_verify(args, rank, ws, local):
         cap = s.kv_prefill + k * n_win + 8
         dec = device_decoder(s, args.seed, cap, dev, mode=args.mode, max_verify=k)
     drafts = synth.bits(args.seed, synth.tensor_id("token", 0, 1), n_win * k) % np.uint64(s.vocab)
-    tok = synth.start_token(args.seed, s.vocab)
+    tok0 = synth.start_token(args.seed, s.vocab)
 
-    def window(i, tok):
-        toks = [int(tok)] + [int(x) for x in drafts[i * k + 1:(i + 1) * k]]
-        am, _ = B.dec_verify(dec.ctx, toks, None, k, s.kv_prefill + i * k, None)
-        return am[-1]
+    def toks_of(i, first):
+        return [int(first)] + [int(x) for x in drafts[i * k + 1:(i + 1) * k]]
 
+    # device-timed: back-to-back windows, no host readback between them
     for i in range(args.warmup):
-        tok = window(i, tok)
+        B.dec_verify(dec.ctx, toks_of(i, tok0), None, k, s.kv_prefill + i * k, None, want_argmax=False)
     barrier(ws)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(dec.stream)
+    for i in range(args.warmup, n_win):
+        B.dec_verify(dec.ctx, toks_of(i, tok0), None, k, s.kv_prefill + i * k, None, want_argmax=False)
+    e1.record(dec.stream)
+    torch.cuda.synchronize()
+    secs = e0.elapsed_time(e1) * 1e-3
+    barrier(ws)
+    B.dec_sync(dec.ctx)
+    # end to end: the model's prediction fed back, argmaxes and status read back every window
+    tok = tok0
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for i in range(args.warmup, n_win):
-        tok = window(i, tok)
-    torch.cuda.synchronize()
-    secs = time.perf_counter() - t0
-    barrier(ws)
+        am, _ = B.dec_verify(dec.ctx, toks_of(i, tok), None, k, s.kv_prefill + i * k, None)
+        tok = am[-1]
+    e2e_secs = time.perf_counter() - t0
     routed = None
     if s.moe:  # distinct routed experts of the last window, averaged over the layers
         routed = float(np.mean([dec.routing(l)["n_slots"] - s.n_shared for l in range(s.n_layers)]))
@@ -374,17 +386,30 @@ def run_verify(args, rank, ws, local):
     per_win = max_over_ranks(secs, ws) / args.steps
     peak, peak_kind = peaks()
     achieved = bytes_win / per_win / 1e9
+    traffic = ncu_traffic(f"{args.workload}_verify{k}", kernel_sources()) if not args.layers else None
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        # the oracle's window is k causal steps: its window tokens/s are its tokens/s
+        cpu = cpu_baseline_layer(s, args.seed)
+        cpu["one_core"] = cpu_baseline_one_core(args.workload, args.seed)
     if rank == 0:
         print(json.dumps({
             "metric": METRIC, "value": whole_job_rate(args.steps * k, secs, ws), "unit": "window tokens/s",
             "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * per_win,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": WORKLOADS[args.workload].format(L=s.n_layers), "verify": k,
-                       "step": f"one verify window of {k} tokens per dec_verify call (host waits for the argmaxes)",
-                       "mode": args.mode, "routed_experts_per_layer": routed},
+                       "step": f"one verify window of {k} tokens (one launch)", "mode": args.mode,
+                       "routed_experts_per_layer": routed,
+                       "l2": "no flush: each window streams %.2f GB > 129 MB L2" % (bytes_win / 1e9)},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                         "peak_kind": peak_kind, "traffic": None, "algorithmic_bytes_per_launch": bytes_win,
+                         "peak_kind": peak_kind, "traffic": traffic, "algorithmic_bytes_per_launch": bytes_win,
+                         "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
                          "kernel": "dec_megakernel (one launch per window)"},
+            "cpu_baseline": cpu,
+            "e2e": {"value": whole_job_rate(args.steps * k, e2e_secs, ws), "unit": "window tokens/s",
+                    "h2d_bytes_per_step": 60 + 4 * k, "d2h_bytes_per_step": 4 * k + 32, "steps": args.steps,
+                    "note": "dec_verify per window: tokens and position copied in, argmaxes and status copied out"},
+            "gpu_launches": args.steps,
         }))
 
 
@@ -454,6 +479,11 @@ def main():
     clk = clocks.stop()
     secs_max = max_over_ranks(secs, ws)
     value = whole_job_rate(args.steps, secs, ws)
+    # five more timed runs after the one the line reports (the median shows the run-to-run spread)
+    Kr = min(args.steps, chain)
+    rep = [timed_generate(dec, dec.ctx, tok0, pos0, Kr, 1, chain)[0] / Kr * 1e3 for _ in range(5)]
+    repeat = {"runs": 5, "steps_each": Kr, "median_ms_per_step": statistics.median(rep),
+              "ms_per_step": [round(x, 4) for x in rep]}
 
     # algorithmic bytes per step averaged over the positions the timed steps used
     poss = [pos0 + (i % chain) for i in range(args.steps)]
@@ -516,6 +546,7 @@ def main():
             "gpu_launches": launches,
             "clocks": clk,
             "compare_launch_modes": compare,
+            "repeat": repeat,
         }
         print(json.dumps(line))
     if ws > 1:

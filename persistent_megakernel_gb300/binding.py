@@ -170,10 +170,15 @@ def dec_generate(ctx: int, token: int, pos: int, n: int, tokens_out=None) -> Non
     check(lib().dec_generate(ctx, token, pos, n, _p(tokens_out)))
 
 
-def dec_verify(ctx: int, tokens, hidden, k: int, pos: int, logits=None):
+def dec_verify(ctx: int, tokens, hidden, k: int, pos: int, logits=None, want_argmax=True):
+    """Returns (argmaxes, accepted count); with want_argmax False the call does not wait and
+    returns None."""
     am = (ctypes.c_int32 * 4)()
     nacc = ctypes.c_int32(0)
     toks = (ctypes.c_int32 * 4)(*(list(tokens) + [0] * (4 - len(tokens)))) if tokens is not None else None
+    if not want_argmax:
+        check(lib().dec_verify(ctx, toks, _p(hidden), k, pos, _p(logits), None, None))
+        return None
     check(lib().dec_verify(ctx, toks, _p(hidden), k, pos, _p(logits), am, ctypes.byref(nacc)))
     return list(am)[:k], nacc.value
 
