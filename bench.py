@@ -4,13 +4,18 @@ Workload (the 2B dense config): 28 layers, hidden 2560, GQA 20 q / 4 kv heads of
 SwiGLU 6912, vocabulary 32768, bf16 weights ~N(0, 0.02) (random init, seeded), bf16 KV cache
 prefilled to 4096 positions ~N(0, 1), greedy steps from a seeded token. A step is one whole
 decode step (embedding row, 28 layers of RMSNorm / QKV / RoPE + KV append / attention /
-o-proj / SwiGLU FFN, final norm, LM head, argmax) -- one launch of the persistent
-megakernel. Steps run in chains of 256 (positions 4096..4351, the workload's 256 greedy
-steps), repeated until K steps are timed.
+o-proj / SwiGLU FFN, final norm, LM head, argmax). Steps run in greedy chains of 256
+(positions 4096..4351, the workload's 256 steps), each chain one launch of the persistent
+megakernel (dec_generate), repeated until K steps are timed.
 
 ``--workload moe_stack`` times the 42-layer MoE stack instead (GQA 20/4 over a 32768-position
 cache, MoE of 512 MXFP4 experts top-8 + 1 shared, FP8 LM head 157184 x 2560, 512 greedy steps
 per chain, positions 32768..33279); its 67 GB of experts are drawn and packed on the device.
+``--token-stream repeat`` feeds the start token at every step instead (one launch per step),
+a stream whose expert routing repeats; the expert prefetch mode comes from the library's
+DEC_EXPERT_PREFETCH (0 off, the default; 1 adaptive; 2 always). ``--verify k`` times k-token verify
+windows. ``--workload dense_layer | moe_layer | lm_head`` times the small configurations cold
+(L2 flushed before every step) and hot.
 
 Prints ONE JSON line (rank 0). Multi-GPU runs are replicas: every rank decodes its own
 request on its own GPU with no communication on the data path; value = all ranks' tokens /
@@ -144,15 +149,32 @@ def sources_sha256(source_files) -> str:
 
 
 def ncu_traffic(key: str, source_files):
-    """DRAM bytes per launch of workload `key` from the committed ncu figures
-    (profiles/dram_traffic.json), if the sources they were taken on are unchanged; else None."""
+    """DRAM bytes (read + write) per decode step, or per verify window, of workload `key` from
+    the committed ncu figures (profiles/dram_traffic.json), if the sources they were taken on are
+    unchanged; else None."""
     p = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if not os.path.exists(p):
         return None
     rec = json.load(open(p)).get(key)
     if not rec:
         return None
-    return float(rec["dram_bytes_per_launch"]) if sources_sha256(source_files) == rec["source_sha256"] else None
+    return float(rec["dram_bytes_per_step"]) if sources_sha256(source_files) == rec["source_sha256"] else None
+
+
+def routing_overlap(dec, s, tok, pos, n, fixed=False):
+    """Mean share of a MoE layer's routed experts that the step before had also chosen, over n
+    one-token steps from (tok, pos), greedy or (fixed) all feeding tok, and every layer
+    (untimed; read from the routing blocks)."""
+    from persistent_megakernel_gb300 import binding as B
+    prev, shares = None, []
+    for i in range(n):
+        nxt = B.dec_step(dec.ctx, tok, None, pos + i, None, True)
+        tok = tok if fixed else nxt
+        cur = [set(dec.routing(l)["expert"][s.n_shared:]) for l in range(s.n_layers)]
+        if prev is not None:
+            shares += [len(a & b) / max(1, len(a)) for a, b in zip(cur, prev)]
+        prev = cur
+    return float(np.mean(shares)) if shares else None
 
 
 def kernel_sources():
@@ -321,6 +343,173 @@ def timed_generate(dec, ctx_handle, tok0, pos0, K, launches_per_step, chain=CHAI
     return e0.elapsed_time(e1) * 1e-3, launches
 
 
+def timed_fixed(dec, tok, pos0, K, chain=CHAIN):
+    """K one-token steps that all feed token `tok` (teacher-forced, no readback), one launch
+    each, at positions pos0 + (i % chain); returns (seconds by CUDA events, launches)."""
+    import torch
+    from persistent_megakernel_gb300 import binding as B
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(dec.stream)
+    launches = 0
+    for i in range(K):
+        B.dec_step(dec.ctx, tok, None, pos0 + (i % chain), None, False)
+        launches += B.dec_last_launch_count(dec.ctx)
+    e1.record(dec.stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e-3, launches
+
+
+SMALL = {
+    "dense_layer": "dense_layer: one dense decoder layer + LM head, hidden 1024, GQA 8/2 x 128, SwiGLU 2816, "
+                   "vocab 32000, 256 cached positions, hidden inputs ~N(0,1)",
+    "moe_layer": "moe_layer: one MoE FFN block, hidden 2560, 512 MXFP4 experts top-8 + 1 shared (intermediate "
+                 "768), bf16 router, hidden inputs ~N(0,1)",
+    "lm_head": "lm_head: final LM head alone, 157184 x 2560 ({dt}), hidden inputs ~N(0,1)",
+}
+
+
+def run_small(args, rank, ws, local):
+    """The small configurations (one dense layer + head, one MoE block, the LM head alone), which
+    fit in L2 or nearly: each step runs on one of 16 seeded inputs in turn (different routings
+    for the MoE block), timed cold, a 256 MB write flushing L2 before every step outside its
+    CUDA events, and hot (steps back to back, weights left in L2 where they fit). e2e: the
+    call a user makes on host buffers: the input copied in from pinned memory, the argmax (or,
+    for the MoE block, dec_run_layer's bf16 output) copied out, every step."""
+    import torch
+    import synth
+    from synth import model as sm
+    from persistent_megakernel_gb300 import build as pbuild
+    pbuild.build()
+    from persistent_megakernel_gb300 import binding as B
+    from persistent_megakernel_gb300 import roofline as R
+    from persistent_megakernel_gb300.model import Decoder
+    from oracle.model import OracleModel, bf16_to_f64_fast
+    from tests.harness import weights
+    k = args.verify
+    dev = f"cuda:{local}"
+    torch.cuda.set_device(local)
+    if args.workload == "dense_layer":
+        s = synth.dense_layer_shape()
+    elif args.workload == "moe_layer":
+        s = synth.moe_layer_shape(verify=k)
+    else:
+        s = synth.lm_head_shape(args.lm_head, verify=k)
+    layers, head, kv, experts = weights(s, args.seed)
+    cap = s.kv_prefill + 8
+    dec = Decoder(s, layers, head, experts=experts, kv=kv, capacity=cap, device=dev, max_verify=k)
+    pos = s.kv_prefill
+    R_IN = 16
+    xs_host = [sm.hidden_inputs(s, args.seed + 100 + i, k) for i in range(R_IN)]
+    xs = [torch.from_numpy(x.view(np.int16)).to(dev) for x in xs_host]
+
+    def one(i):
+        if k == 1:
+            B.dec_step(dec.ctx, 0, xs[i % R_IN], pos, None, False)
+        else:
+            B.dec_verify(dec.ctx, None, xs[i % R_IN], k, pos, None, want_argmax=False)
+
+    routed = None
+    if s.moe:  # distinct routed experts per step, averaged over the inputs
+        n = []
+        for i in range(R_IN):
+            one(i)
+            n.append(dec.routing(0)["n_slots"] - s.n_shared)
+        routed = float(np.mean(n))
+    bytes_step = R.algorithmic_bytes(s, pos, m=k, n_routed_active=None if routed is None else routed)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    K = args.steps
+    for i in range(args.warmup):
+        one(i)
+    clocks = Clocks(local)
+    clocks.start()
+    barrier(ws)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    with torch.cuda.stream(dec.stream):
+        for i in range(K):
+            flush.fill_(i & 255)
+            ev[i][0].record(dec.stream)
+            one(i)
+            ev[i][1].record(dec.stream)
+    torch.cuda.synchronize()
+    cold = sum(a.elapsed_time(b) for a, b in ev) * 1e-3
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(dec.stream)
+    for i in range(K):
+        one(i)
+    e1.record(dec.stream)
+    torch.cuda.synchronize()
+    hot = e0.elapsed_time(e1) * 1e-3
+    barrier(ws)
+    clk = clocks.stop()
+    cold_max = max_over_ranks(cold, ws)
+    # end to end through the C ABI on host buffers
+    pin = [torch.from_numpy(x.view(np.int16)).pin_memory() for x in xs_host]
+    xin = torch.empty_like(xs[0])
+    hout = torch.empty((k, s.hidden), dtype=torch.int16, device=dev)
+    hout_host = torch.empty((k, s.hidden), dtype=torch.int16).pin_memory()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(K):
+        with torch.cuda.stream(dec.stream):
+            xin.copy_(pin[i % R_IN], non_blocking=True)
+        if s.moe:
+            B.dec_run_layer(dec.ctx, 0, xin, k, pos, hout)
+            with torch.cuda.stream(dec.stream):
+                hout_host.copy_(hout, non_blocking=True)
+            dec.stream.synchronize()
+        elif k == 1:
+            B.dec_step(dec.ctx, 0, xin, pos, None, True)
+        else:
+            B.dec_verify(dec.ctx, None, xin, k, pos, None)
+    e2e_secs = time.perf_counter() - t0
+    d2h = 2 * k * s.hidden if s.moe else 4 * k + 32
+    # the oracle on one token of the same configuration, as it stands, on the host cores
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        orc = OracleModel(s, layers, head, experts=experts, kv=kv, capacity=cap)
+        xf = bf16_to_f64_fast(xs_host[0][0])
+        orc.step(xf, pos)
+        n_done, t0 = 0, time.perf_counter()
+        while n_done < 3 or time.perf_counter() - t0 < 5.0:
+            orc.step(bf16_to_f64_fast(xs_host[n_done % R_IN][0]), pos)
+            n_done += 1
+        per = (time.perf_counter() - t0) / n_done
+        cpu = {"value": 1.0 / per, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"{n_done} one-token steps of the fp64 numpy oracle on this configuration: {per:.3f} s each"}
+    if rank == 0:
+        peak, peak_kind = peaks()
+        per_cold = cold_max / K
+        achieved = bytes_step / per_cold / 1e9
+        unit = "tokens/s" if k == 1 else "window tokens/s"
+        print(json.dumps({
+            "metric": METRIC, "value": whole_job_rate(K * k, cold, ws), "unit": unit, "n_gpus": ws, "steps": K,
+            "warmup": args.warmup, "ms_per_step": 1e3 * per_cold, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": SMALL[args.workload].format(dt=args.lm_head), "verify": k, "mode": "persistent",
+                       "routed_experts_per_step": routed,
+                       "l2": "cold: a 256 MB write flushes L2 before every step, outside the step's CUDA events; "
+                             "16 seeded inputs in turn",
+                       "parallelism": f"replicas x{ws}"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                         "peak_kind": peak_kind, "traffic": None, "algorithmic_bytes_per_launch": bytes_step,
+                         "launch_us": 1e6 * per_cold, "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
+                         "kernel": "dec_megakernel (one launch per step)"},
+            "hot_l2": {"value": whole_job_rate(K * k, hot, ws), "unit": unit, "ms_per_step": 1e3 * hot / K,
+                       "achieved_gbs": bytes_step / (hot / K) / 1e9,
+                       "note": "steps back to back: weights that fit stay in L2 (not a bandwidth figure)"},
+            "cpu_baseline": cpu,
+            "e2e": {"value": whole_job_rate(K * k, e2e_secs, ws), "unit": unit,
+                    "h2d_bytes_per_step": 2 * k * s.hidden + 60, "d2h_bytes_per_step": d2h, "steps": K,
+                    "note": ("dec_run_layer" if s.moe else ("dec_step" if k == 1 else "dec_verify")) +
+                            " per step: the input copied in from pinned host memory, the result copied out"},
+            "gpu_launches": K,
+            "clocks": clk,
+        }))
+
+
 def run_verify(args, rank, ws, local):
     """Verify windows of k tokens (the MTP verify step of the Ling-3.0-flash DGX Spark article,
     "optimisation 3"): each call feeds k tokens at the next k positions (positions advance by k,
@@ -386,7 +575,7 @@ def run_verify(args, rank, ws, local):
     per_win = max_over_ranks(secs, ws) / args.steps
     peak, peak_kind = peaks()
     achieved = bytes_win / per_win / 1e9
-    traffic = ncu_traffic(f"{args.workload}_verify{k}", kernel_sources()) if not args.layers else None
+    traffic = ncu_traffic(f"{args.workload}_verify{k}", kernel_sources()) if not args.layers else None  # per window
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         # the oracle's window is k causal steps: its window tokens/s are its tokens/s
@@ -403,6 +592,7 @@ def run_verify(args, rank, ws, local):
                        "l2": "no flush: each window streams %.2f GB > 129 MB L2" % (bytes_win / 1e9)},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                          "peak_kind": peak_kind, "traffic": traffic, "algorithmic_bytes_per_launch": bytes_win,
+                         "launch_us": 1e6 * per_win,
                          "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
                          "kernel": "dec_megakernel (one launch per window)"},
             "cpu_baseline": cpu,
@@ -423,10 +613,14 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-compare", action="store_true", help="skip the launch-per-op comparison")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", default="dense_2b", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="dense_2b", choices=sorted(WORKLOADS) + sorted(SMALL))
+    ap.add_argument("--lm-head", default="bf16", choices=["bf16", "fp8"], help="--workload lm_head: its format")
     ap.add_argument("--verify", type=int, default=1, choices=[1, 2, 3, 4],
                     help="> 1: time verify windows of this many tokens")
     ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"], help="KV cache format (fp8: e4m3, scales 1.0)")
+    ap.add_argument("--token-stream", default="greedy", choices=["greedy", "repeat"],
+                    help="repeat: every step feeds the start token (teacher-forced, one launch per step), "
+                         "a stream whose MoE routing repeats from step to step")
     ap.add_argument("--cpu-one-core", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling captures only: fewer decoder layers (the line is then not the workload's)")
@@ -437,9 +631,13 @@ def main():
         print(json.dumps(cpu_baseline_layer(workload_shape(args.workload), args.seed)))
         return
     if args.impl == "reference":
+        if args.workload in SMALL:
+            ap.error("--impl reference times dense_2b or moe_stack (a small workload's line carries its oracle's time)")
         return run_reference(args)
 
     rank, ws, local = dist_setup(args.gpus)
+    if args.workload in SMALL:
+        return run_small(args, rank, ws, local)
     if args.verify > 1:
         return run_verify(args, rank, ws, local)
     import torch
@@ -468,12 +666,17 @@ def main():
     pos0 = s.kv_prefill
 
     # warm-up, then exactly K timed steps bracketed by barrier + synchronize
-    timed_generate(dec, dec.ctx, tok0, pos0, args.warmup, 1, chain)
+    fixed = args.token_stream == "repeat"
+
+    def run_steps(K):
+        return timed_fixed(dec, tok0, pos0, K, chain) if fixed else timed_generate(dec, dec.ctx, tok0, pos0, K, 1, chain)
+
+    run_steps(args.warmup)
     clocks = Clocks(local)
     clocks.start()
     barrier(ws)
     torch.cuda.synchronize()
-    secs, launches = timed_generate(dec, dec.ctx, tok0, pos0, args.steps, 1, chain)
+    secs, launches = run_steps(args.steps)
     torch.cuda.synchronize()
     barrier(ws)
     clk = clocks.stop()
@@ -481,18 +684,24 @@ def main():
     value = whole_job_rate(args.steps, secs, ws)
     # five more timed runs after the one the line reports (the median shows the run-to-run spread)
     Kr = min(args.steps, chain)
-    rep = [timed_generate(dec, dec.ctx, tok0, pos0, Kr, 1, chain)[0] / Kr * 1e3 for _ in range(5)]
+    rep = [run_steps(Kr)[0] / Kr * 1e3 for _ in range(5)]
     repeat = {"runs": 5, "steps_each": Kr, "median_ms_per_step": statistics.median(rep),
               "ms_per_step": [round(x, 4) for x in rep]}
 
-    # algorithmic bytes per step averaged over the positions the timed steps used
+    # algorithmic bytes per step averaged over the positions the timed steps used; one launch runs
+    # a chain of steps, so per launch: bytes per step x steps per launch over the launch's time
     poss = [pos0 + (i % chain) for i in range(args.steps)]
     bytes_step = float(np.mean([R.algorithmic_bytes(s, p) for p in poss]))
+    steps_per_launch = args.steps / launches
     launch_s = secs / launches
     peak, peak_kind = peaks()
-    achieved = bytes_step * (1 if args.mode == "persistent" else 1) / (secs / args.steps) / 1e9
+    achieved = bytes_step * steps_per_launch / launch_s / 1e9
     traffic_key = args.workload + ("_kv8" if args.kv == "fp8" else "")
-    traffic = ncu_traffic(traffic_key, kernel_sources()) if args.mode == "persistent" and not args.layers else None
+    traffic_step = ncu_traffic(traffic_key, kernel_sources()) if args.mode == "persistent" and not args.layers else None
+    traffic = traffic_step * steps_per_launch if traffic_step is not None else None
+    overlap = None
+    if s.moe and rank == 0:
+        overlap = routing_overlap(dec, s, tok0, pos0, 9, fixed)
 
     # end to end through the C ABI with host buffers: token in, argmax out, every step
     K2 = min(args.steps, chain)
@@ -500,7 +709,8 @@ def main():
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for i in range(K2):
-        tok = B.dec_step(dec.ctx, tok, None, pos0 + i, None, True)
+        nxt = B.dec_step(dec.ctx, tok, None, pos0 + i, None, True)
+        tok = tok if fixed else nxt
     e2e_secs = time.perf_counter() - t0
     e2e = {"value": whole_job_rate(K2, e2e_secs, ws), "unit": "tokens/s", "h2d_bytes_per_step": 60, "d2h_bytes_per_step": 36,
            "steps": K2, "note": "dec_step per token: token and position copied in, argmax and status copied out"}
@@ -538,9 +748,12 @@ def main():
                        "parallelism": f"replicas x{ws}"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": peak_kind, "traffic": traffic,
-                         "algorithmic_bytes_per_launch": bytes_step, "launch_us": launch_s * 1e6,
+                         "traffic_per_step": traffic_step,
+                         "algorithmic_bytes_per_launch": bytes_step * steps_per_launch,
+                         "algorithmic_bytes_per_step": bytes_step, "steps_per_launch": steps_per_launch,
+                         "launch_us": launch_s * 1e6, "step_us": 1e6 * secs / args.steps,
                          "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
-                         "kernel": "dec_megakernel (one launch per decode step)"},
+                         "kernel": "dec_megakernel (one launch per chain of greedy steps)"},
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": launches,
@@ -548,6 +761,13 @@ def main():
             "compare_launch_modes": compare,
             "repeat": repeat,
         }
+        if fixed:
+            line["config"]["token_stream"] = ("repeat: every step feeds the start token at the next position "
+                                              "(teacher-forced, one launch per step)")
+        if s.moe:
+            line["config"]["expert_prefetch"] = {
+                "mode": int(os.environ.get("DEC_EXPERT_PREFETCH", "0")),
+                "routed_overlap_with_previous_step": overlap}
         print(json.dumps(line))
     if ws > 1:
         import torch.distributed as dist

@@ -126,7 +126,12 @@ size_t dec_workspace_bytes(const dec_config* cfg);
 
 /* Validate cfg, bind the CUDA stream (cudaStream_t, NULL = legacy default) and the
    caller's workspace (dec_workspace_bytes long, 256-byte aligned, any contents: it is
-   cleared here), and create a context on the current device. */
+   cleared here), and create a context on the current device. The environment variable
+   DEC_EXPERT_PREFETCH, read here, sets the MoE expert prefetch (the Muse Spark Open
+   megakernel article prefetches the experts the previous step routed to): while a layer's
+   routing is pending, ask L2 for 0: nothing (the default), 1: the shared experts, plus the
+   experts the layer's last routing chose when at least half of them had been chosen by the
+   routing before it, 2: both, always. Results do not depend on it. */
 dec_status dec_init(const dec_config* cfg, void* cuda_stream, void* workspace_dev, dec_ctx** out);
 
 /* Register packed weight tensors (device pointers, caller-owned and kept alive until

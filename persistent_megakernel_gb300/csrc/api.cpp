@@ -8,6 +8,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <string>
 #include <vector>
@@ -70,8 +71,8 @@ struct LayerW {
 constexpr int kMaxSubOps = 8;  // ops of one layer (at most 7) or of the LM head alone
 
 struct Layout {  // byte offsets into the workspace
-  size_t state, status, tickets, ctr, ops, subops, wops, tmaps, hs, qkv, attn_out, hbuf, rlogits, route, eh, part, logits, am_val, am_idx,
-      am_out, trace, total;
+  size_t state, status, tickets, ctr, ops, subops, wops, tmaps, hs, qkv, attn_out, hbuf, rlogits, route, xpf, eh, part, logits, am_val,
+      am_idx, am_out, trace, total;
   int n_ops, n_tickets, n_ctas, ns_max, slot_bytes, act_bytes, exp_stage_all;
 };
 
@@ -255,6 +256,7 @@ bool compute_layout(const dec_config* c, Layout& L, std::string& why) {
   L.hbuf = take((size_t)nl * M * c->ffn * 8);
   L.rlogits = take((size_t)nl * M * c->n_experts * 8);
   L.route = take((size_t)(c->n_experts ? nl : 0) * sizeof(RouteBlock));
+  L.xpf = take((size_t)(c->n_experts ? nl : 0) * kXpfWords * 4);
   L.eh = take((size_t)(c->n_experts ? nl : 0) * kMaxRouteSlots * M * c->moe_inter * 8);
   L.part = take((size_t)(c->n_q ? nl * c->n_kv : 0) * L.ns_max * M * G * kPart * 8);
   L.logits = take((size_t)M * c->vocab * 4);
@@ -292,6 +294,7 @@ struct dec_ctx {
   dec_status sticky_code = DEC_OK;
   cudaGraphExec_t graph = nullptr;
   int attn_tc = 0;                   // tensor-core attention (tensor maps below encoded)
+  int xpf_mode = 0;                  // expert prefetch (DEC_EXPERT_PREFETCH: 0 off, 1 adaptive, 2 always)
   std::vector<OpDesc> wops;          // the op list of multi-token calls (max_verify > 1)
   KParams wkp;
   std::vector<CUtensorMap> tmaps_host;  // the tensor maps of its tensor-core ops
@@ -532,6 +535,7 @@ struct ListBuilder {
     if (g.n_experts) {
       const int I = g.moe_inter, E = g.n_experts;
       int32_t* route = reinterpret_cast<int32_t*>(wsp<uint8_t>(c, L.route) + (size_t)l * sizeof(RouteBlock));
+      int32_t* xpf = wsp<int32_t>(c, L.xpf) + (size_t)l * kXpfWords;
       uint64_t* eh = wsp<uint64_t>(c, L.eh) + (size_t)l * kMaxRouteSlots * M * I;
       uint64_t* rlogits = wsp<uint64_t>(c, L.rlogits) + (size_t)l * M * E;
       const int64_t gu_v = (int64_t)2 * I * (H / 2), gu_s = (int64_t)2 * I * (H / 32);
@@ -548,6 +552,7 @@ struct ListBuilder {
       r.out = rlogits;
       r.act = rlogits;  // routing ops read the layer's router logits
       r.route = route;
+      r.xpf = xpf;
       r.aux_ctr = r.ctr;  // the routing waits for every CTA's logits
       geom(r);
       ops.push_back(r);
@@ -569,6 +574,7 @@ struct ListBuilder {
       rg.slot1 = -1;
       rg.eh = eh;
       rg.route = route;
+      rg.xpf = xpf;
       rg.act = rlogits;
       rg.wait_ctr = x_ready;  // its own input is x'; its routing waits for the router (aux)
       rg.aux_ctr = r.ctr;
@@ -586,6 +592,7 @@ struct ListBuilder {
       dn.ws_mstride = dn_s;
       dn.eh = eh;
       dn.route = route;
+      dn.xpf = xpf;
       dn.act = rlogits;
       dn.wait_ctr = rg.ctr;  // routed (and, earlier in every CTA, shared) expert hidden vectors
       dn.aux_ctr = r.ctr;
@@ -662,6 +669,7 @@ void fill_params(dec_ctx* c, KParams& k, size_t ops_off, int n_ops) {
   k.slot_bytes = L.slot_bytes;
   k.act_bytes = L.act_bytes;
   k.kv_fp8 = g.kv_dtype == DEC_FP8_E4M3 ? 1 : 0;
+  k.xpf_mode = c->xpf_mode;
   k.attn_tc = c->attn_tc;
   k.attn_window = g.attn_window;
   k.tmap_k = c->tmap_k;
@@ -937,6 +945,10 @@ dec_status dec_init(const dec_config* cfg, void* cuda_stream, void* workspace_de
   c->ws = static_cast<uint8_t*>(workspace_dev);
   c->lay = L;
   c->layers.resize(cfg->n_layers);
+  if (const char* v = std::getenv("DEC_EXPERT_PREFETCH")) {
+    const int m = std::atoi(v);
+    c->xpf_mode = m < 0 ? 0 : (m > 2 ? 2 : m);
+  }
   cudaError_t e = cudaMemsetAsync(c->ws, 0, L.total, c->stream);
   if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);
   if (e != cudaSuccess) {

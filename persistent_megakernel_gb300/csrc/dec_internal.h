@@ -33,6 +33,9 @@ constexpr int kRmax = 8;                         // rows one warp accumulates pe
 constexpr int kMmax = 4;                         // tokens per call (verify window)
 constexpr int kHeadDim = 128;
 constexpr int kMaxRouteSlots = 1 + 8 * kMmax;    // shared + union of routed experts
+// Expert prefetch record of one MoE layer (int32 words): routed experts the layer's last routing
+// shared with the one before it, slots of the last routing, then its expert ids (shared first).
+constexpr int kXpfWords = 2 + kMaxRouteSlots + 1;  // padded to a multiple of 4 words
 constexpr int kPart = 132;                       // attention partial: max, sum, 2 pad, output[128]
 constexpr int kMaxSlotBytes = 16384;             // one warp's ring slot at most (attention rows <= 32)
 constexpr int kSmemLimit = 232448;               // dynamic shared memory per CTA on sm_103a
@@ -91,6 +94,7 @@ struct OpDesc {
   const CUtensorMap* tmap;            // tc ops: the weight matrix as a 2D tensor (K columns x N rows),
                                       // boxes of 64 columns x kGemvTcRows rows, 128-byte swizzle
   int32_t kw, pad1;                   // column split: columns per warp (0: Kc, in one tile)
+  int32_t* xpf;                       // MoE ops: this layer's expert prefetch record (kXpfWords)
 };
 
 struct RouteBlock {
@@ -128,7 +132,10 @@ struct KParams {
   float eps, rope_base;
   uint64_t timeout_ns;
   int32_t slot_bytes, act_bytes;      // bytes of one warp's ring slot; shared-memory scratch
-  int32_t kv_fp8, pad1;               // 1: the KV cache holds e4m3 codes (128 B per row), else bf16
+  int32_t kv_fp8;                     // 1: the KV cache holds e4m3 codes (128 B per row), else bf16
+  int32_t xpf_mode;                   // expert prefetch while the routing is pending: 0 off, 1 the
+                                      // shared experts, plus the last routing's experts when at least
+                                      // half of them repeated the routing before it; 2 both always
   StepState* state;
   Status* status;
   uint32_t* tickets;

@@ -617,6 +617,57 @@ struct Producer {
     }
   }
 
+  // Ask L2 for lane gl's share (of nl) of a byte range, in 16-byte granules (an unaligned range
+  // is left to the copies).
+  __device__ __forceinline__ void prefetch_share(const char* base, size_t bytes, int gl, int nl) {
+    if (reinterpret_cast<uintptr_t>(base) & 15u) return;
+    const size_t granules = bytes / 16, per = (granules + (size_t)nl - 1) / (size_t)nl;
+    const size_t g0 = (size_t)gl * per;
+    if (g0 >= granules) return;
+    const size_t g1 = granules < g0 + per ? granules : g0 + per;
+    prefetch_l2(base + g0 * 16, (uint32_t)((g1 - g0) * 16));
+  }
+
+  // Lane gl's share of expert e's matrix (values and scales) of an expert op.
+  __device__ __forceinline__ void prefetch_expert(const OpDesc* op, int e, int gl, int nl) {
+    const int K = __ldg(&op->K), N = __ldg(&op->N), wt = __ldg(&op->wtype);
+    prefetch_share(static_cast<const char*>(op->w) + (size_t)e * __ldg(&op->w_mstride), (size_t)N * row_bytes(wt, K), gl, nl);
+    if (wt == W_MXFP4)
+      prefetch_share(static_cast<const char*>(op->ws) + (size_t)e * __ldg(&op->ws_mstride), (size_t)N * (K / 32), gl, nl);
+  }
+
+  // Expert prefetch (the Muse Spark Open megakernel article prefetches the experts the previous
+  // step routed to): while cursor c waits at a routed gate/up op for the layer's routing, the
+  // lanes of all CTAs ask L2 for the gate/up and down matrices of the shared experts, always
+  // needed, and of the experts the layer's last routing chose, when at least half of those had
+  // also been chosen by the routing before it (xpf_mode 1; 2: always). Once per op and step.
+  __device__ __forceinline__ bool expert_prefetch(const LaneCursor& c, int w, int& key) {
+    if (c.oi >= p.op_end) return false;
+    const OpDesc* op = p.ops + c.oi;
+    if (__ldg(&op->type) != OP_ROUTED_GATEUP) return false;
+    const int32_t* rec = op->xpf;
+    if (!rec) return false;
+    const int k = c.step * p.n_ops + c.oi;
+    if (k == key) return false;
+    key = k;
+    const OpDesc* dn = (c.oi + 1 < p.op_end && __ldg(&p.ops[c.oi + 1].type) == OP_EXP_DOWN) ? op + 1 : nullptr;
+    const int gl = blockIdx.x * kConsumerWarps + w, nl = p.n_ctas * kConsumerWarps;
+    for (int sh = 0; sh < p.n_shared; ++sh) {
+      prefetch_expert(op, p.E + sh, gl, nl);
+      if (dn) prefetch_expert(dn, p.E + sh, gl, nl);
+    }
+    const int hits = ld_relaxed_s32(rec), n = min(ld_relaxed_s32(rec + 1), kMaxRouteSlots);
+    const int routed = n - p.n_shared;
+    if (routed > 0 && (p.xpf_mode == 2 || 2 * hits >= routed))
+      for (int j = p.n_shared; j < n; ++j) {
+        const int e = ld_relaxed_s32(rec + 2 + j);
+        if (e < 0 || e >= p.E) continue;  // a torn or stale record: a hint only
+        prefetch_expert(op, e, gl, nl);
+        if (dn) prefetch_expert(dn, e, gl, nl);
+      }
+    return true;
+  }
+
   // Bytes a tile brings into its slot.
   __device__ __forceinline__ uint32_t tile_bytes(const OpDesc* op, int type, const Tile& t) const {
     if (type == OP_ATTN) return (uint32_t)(t.nr * 2 * kv_row_bytes(p.kv_fp8));
@@ -713,6 +764,7 @@ struct Producer {
     c.n = 0;
     LaneCursor pf = c;  // L2-prefetch cursor: at or ahead of the ring's
     uint32_t pf_n = 0;
+    int xpf_key = -1;   // (step, op) of the last expert prefetch
     uint64_t t_idle = 0;
     for (;;) {
       Tile t;
@@ -745,13 +797,17 @@ struct Producer {
         AttnIter pa2;
         GemvIter pg2;
         bool did = false;
-        if (pf_n < c.n + (uint32_t)DEC_L2_AHEAD && peek(pf, w, tp, pa2, pg2)) {
-          const int ptype = __ldg(&p.ops[pf.oi].type);
-          prefetch_tile(p.ops + pf.oi, ptype, tp);
-          if (ptype == OP_ATTN) pf.a = pa2;
-          else pf.g = pg2;
-          ++pf_n;
-          did = true;
+        if (pf_n < c.n + (uint32_t)DEC_L2_AHEAD) {
+          if (peek(pf, w, tp, pa2, pg2)) {
+            const int ptype = __ldg(&p.ops[pf.oi].type);
+            prefetch_tile(p.ops + pf.oi, ptype, tp);
+            if (ptype == OP_ATTN) pf.a = pa2;
+            else pf.g = pg2;
+            ++pf_n;
+            did = true;
+          } else if (p.xpf_mode) {
+            did = expert_prefetch(pf, w, xpf_key);  // the cursor waits for a routing
+          }
         }
         if (__any_sync(kMask, did)) continue;
       }
@@ -1339,6 +1395,32 @@ struct Consumer {
       s.flags[kFlagRoute] = route_tag(epoch, op.layer, p.L);  // the producer lanes may now read the ids
     }
     consumer_sync();
+    if (op.xpf && blockIdx.x == p.n_ctas - 1 && warp == 0) {
+      // the layer's expert prefetch record, a hint the producers of every CTA read with relaxed
+      // loads: how many of this routing's routed experts the layer's last routing also chose, the
+      // slot count, then this routing's expert ids
+      const int n = rb->n_slots, ns = p.n_shared;
+      const int pn = min(max(ld_relaxed_s32(op.xpf + 1), 0), kMaxRouteSlots);
+      const int pa = lane < pn ? ld_relaxed_s32(op.xpf + 2 + lane) : -1;
+      const int pb = pn > 32 ? ld_relaxed_s32(op.xpf + 2 + 32) : -1;
+      const int c0 = (lane >= ns && lane < n) ? rb->expert[lane] : -2;
+      const int c1 = (lane + 32 >= ns && lane + 32 < n) ? rb->expert[lane + 32] : -2;
+      bool f0 = false, f1 = false;
+      for (int q = ns; q < pn; ++q) {
+        const int e = __shfl_sync(0xffffffffu, pa, q & 31);
+        const int pe = q < 32 ? e : pb;
+        f0 |= pe == c0;
+        f1 |= pe == c1;
+      }
+      const int hits = __popc(__ballot_sync(0xffffffffu, f0)) + __popc(__ballot_sync(0xffffffffu, f1));
+      __syncwarp();
+      if (lane < n) st_relaxed_s32(op.xpf + 2 + lane, rb->expert[lane]);
+      if (lane + 32 < n) st_relaxed_s32(op.xpf + 2 + 32 + lane, rb->expert[lane + 32]);
+      if (lane == 0) {
+        st_relaxed_s32(op.xpf, hits);
+        st_relaxed_s32(op.xpf + 1, n);
+      }
+    }
     if (blockIdx.x == 0) {  // a copy in global memory for inspection
       const int* src = reinterpret_cast<const int*>(rb);
       for (int i = tid; i < (int)(sizeof(RouteBlock) / 4); i += kConsumerThreads) op.route[i] = src[i];

@@ -85,3 +85,34 @@ def test_moe_layer_verify_window(moe):
     xd = torch.from_numpy(xs.view(np.int16)).cuda()
     dec.verify(None, 0, hidden=xd, k=4)
     _check(dec, orc, xs, 4)
+
+
+def test_expert_prefetch_modes_agree(moe):
+    """The expert prefetch (DEC_EXPERT_PREFETCH: 0 off, 1 adaptive, 2 always) is an L2 hint and
+    leaves every result bit for bit unchanged. A repeated input gives the adaptive mode's
+    locality rule routed experts to prefetch on the steps after the first."""
+    import os
+    import torch
+    seed, xs, _, orc = moe
+    w = weights(SHAPE, seed)
+    seq = [0, 0, 1, 0, 0]  # hidden inputs of consecutive one-token steps, positions 0..4
+    runs = {}
+    old = os.environ.get("DEC_EXPERT_PREFETCH")
+    try:
+        for mode in ("0", "1", "2"):
+            os.environ["DEC_EXPERT_PREFETCH"] = mode
+            dec = decoder_for(SHAPE, seed, 8, w=w, max_verify=4)
+            out = []
+            for pos, i in enumerate(seq):
+                dec.step(0, pos, hidden=torch.from_numpy(xs[i:i + 1].view(np.int16)).cuda())
+                out.append(dec.hidden_stream()[2][0].cpu().numpy().copy())
+            dec.close()
+            runs[mode] = np.stack(out)
+    finally:
+        if old is None:
+            os.environ.pop("DEC_EXPERT_PREFETCH", None)
+        else:
+            os.environ["DEC_EXPERT_PREFETCH"] = old
+    assert np.array_equal(runs["0"], runs["1"]) and np.array_equal(runs["0"], runs["2"])
+    inf = orc.step(bf16_to_f64_fast(xs[0]), 0)
+    assert rel_err(runs["2"][0], inf["x_out"]) <= TOL
