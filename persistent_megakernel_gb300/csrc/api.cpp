@@ -74,6 +74,7 @@ struct Layout {  // byte offsets into the workspace
   size_t state, status, tickets, ctr, ops, subops, wops, tmaps, hs, qkv, attn_out, hbuf, rlogits, route, xpf, eh, part, logits, am_val,
       am_idx, am_out, trace, total;
   int n_ops, n_tickets, n_ctas, ns_max, slot_bytes, act_bytes, exp_stage_all;
+  int slot1_bytes, act1_bytes, exp_stage_all1;  // the one-token list's geometry
 };
 
 bool validate(const dec_config* c, std::string& why) {
@@ -191,47 +192,54 @@ bool compute_layout(const dec_config* c, Layout& L, std::string& why) {
   L.ns_max = c->n_q ? std::max(1, C / c->n_kv / DEC_ATTN_SPLIT_DIV) : 1;
   L.n_tickets = 2;  // LM-head argmax, step end
 
-  // shared-memory scratch ("act") the largest op needs, in floats; a multi-token list's
-  // tensor-core ops stage their inputs in kMmax tokens' bytes whatever the window
+  // Shared-memory geometry of a list whose calls carry up to Mg tokens: the scratch ("act") its
+  // largest op needs, in floats (a multi-token list's tensor-core ops stage their inputs in
+  // kMmax tokens' bytes whatever the window), and the ring slots the rest leaves.
   const int rows_cta = (H + C - 1) / C + 16;
-  const int Ma = M > 1 ? kMmax : 1;
-  size_t act = (size_t)Ma * H;
-  act = std::max(act, (size_t)2 * kConsumerThreads);
-  if (c->n_q) {
-    const size_t MG = (size_t)M * G;
-    act = std::max(act, (size_t)Ma * c->n_q * kHeadDim + (size_t)rows_cta * M * (1 + kConsumerWarps));
-    // the attention scratch the kernel carves (at most 32 KV rows per ring slot)
-    (void)MG;
-    act = std::max(act, (size_t)attn_layout(M, G, kMaxSlotBytes / 512, L.ns_max).end);
-  }
-  if (c->ffn) act = std::max(act, (size_t)Ma * c->ffn + (size_t)rows_cta * M * (1 + kConsumerWarps));
-  act = std::max(act, (size_t)Ma * H + (size_t)2 * (rows_cta + 1) * M * kConsumerWarps);  // column-split partials
-  L.exp_stage_all = 0;
-  if (c->n_experts) {
-    act = std::max(act, (size_t)M * c->n_experts);
-    const size_t per_slot = (size_t)M * c->moe_inter + 2 * (size_t)rows_cta * M;
-    // every slot's hidden vectors, the residual rows and one set of partial sums per warp
-    const size_t all = (size_t)(c->n_shared + c->top_k * M) * M * c->moe_inter + (1 + kConsumerWarps) * (size_t)rows_cta * M;
-    if (all <= std::max(act, (size_t)7168)) {
-      act = std::max(act, all);
-      L.exp_stage_all = 1;
-    } else {
-      act = std::max(act, per_slot);
+  auto geometry = [&](int Mg, int& slot_bytes, int& act_bytes, int& stage_all) -> bool {
+    const int Ma = Mg > 1 ? kMmax : 1;
+    size_t act = (size_t)Ma * H;
+    act = std::max(act, (size_t)2 * kConsumerThreads);
+    if (c->n_q) {
+      act = std::max(act, (size_t)Ma * c->n_q * kHeadDim + (size_t)rows_cta * Mg * (1 + kConsumerWarps));
+      // the attention scratch the kernel carves (at most 32 KV rows per ring slot)
+      act = std::max(act, (size_t)attn_layout(Mg, G, kMaxSlotBytes / 512, L.ns_max).end);
     }
-  }
-  act = align_up(act * 4, 256);
-  const int common = dec_megakernel_common_bytes();
-  const long long room = (long long)kSmemLimit - (long long)act - common;
-  // ring slots: 256-byte multiples, 1024 when tensor copies with a 128-byte swizzle land in them
-  const int slot_align = (attn_tc_for(c) || c->max_verify > 1) ? 1024 : 256;
-  long long slot = room / (kConsumerWarps * kStages) / slot_align * slot_align;
-  slot = std::min<long long>(slot, kMaxSlotBytes);
-  if (slot < 4096) {
+    if (c->ffn) act = std::max(act, (size_t)Ma * c->ffn + (size_t)rows_cta * Mg * (1 + kConsumerWarps));
+    act = std::max(act, (size_t)Ma * H + (size_t)2 * (rows_cta + 1) * Mg * kConsumerWarps);  // column-split partials
+    stage_all = 0;
+    if (c->n_experts) {
+      act = std::max(act, (size_t)Mg * c->n_experts);
+      const size_t per_slot = (size_t)Mg * c->moe_inter + 2 * (size_t)rows_cta * Mg;
+      // every slot's hidden vectors, the residual rows and one set of partial sums per warp
+      const size_t all =
+          (size_t)(c->n_shared + c->top_k * Mg) * Mg * c->moe_inter + (1 + kConsumerWarps) * (size_t)rows_cta * Mg;
+      if (all <= std::max(act, (size_t)7168)) {
+        act = std::max(act, all);
+        stage_all = 1;
+      } else {
+        act = std::max(act, per_slot);
+      }
+    }
+    act = align_up(act * 4, 256);
+    const int common = dec_megakernel_common_bytes();
+    const long long room = (long long)kSmemLimit - (long long)act - common;
+    // ring slots: 256-byte multiples, 1024 when tensor copies with a 128-byte swizzle land in them
+    const int slot_align = (attn_tc_for(c) || c->max_verify > 1) ? 1024 : 256;
+    long long slot = room / (kConsumerWarps * kStages) / slot_align * slot_align;
+    slot = std::min<long long>(slot, kMaxSlotBytes);
+    if (slot < 4096) return false;
+    slot_bytes = (int)slot;
+    act_bytes = (int)act;
+    return true;
+  };
+  // multi-token calls (and the layer-level entry points) use the max_verify geometry; one-token
+  // steps run a list of their own with the smaller scratch of one token and larger ring slots
+  if (!geometry(M, L.slot_bytes, L.act_bytes, L.exp_stage_all) ||
+      !geometry(1, L.slot1_bytes, L.act1_bytes, L.exp_stage_all1)) {
     why = "shapes need more shared memory than a CTA has";
     return false;
   }
-  L.slot_bytes = (int)slot;
-  L.act_bytes = (int)act;
 
   size_t o = 0;
   auto take = [&](size_t bytes) {
@@ -366,9 +374,18 @@ struct ListBuilder {
   std::vector<OpDesc>& ops;
   int xsrc, x_idx, prev;
   bool window = false;               // a multi-token list: bf16 matrices on tensor-core tiles
+  int gm;                            // tokens the list's geometry serves: 1, or max_verify
+  int slot, act, stage_all;          // its ring slot and scratch bytes, expert-down staging
   dec_status err = DEC_OK;
 
-  ListBuilder(dec_ctx* c_, std::vector<OpDesc>& ops_, int xsrc_) : c(c_), ops(ops_), xsrc(xsrc_), x_idx(0), prev(-1) {}
+  ListBuilder(dec_ctx* c_, std::vector<OpDesc>& ops_, int xsrc_, bool one_token = false)
+      : c(c_), ops(ops_), xsrc(xsrc_), x_idx(0), prev(-1) {
+    const Layout& L = c->lay;
+    gm = one_token ? 1 : c->cfg.max_verify;
+    slot = one_token ? L.slot1_bytes : L.slot_bytes;
+    act = one_token ? L.act1_bytes : L.act_bytes;
+    stage_all = one_token ? L.exp_stage_all1 : L.exp_stage_all;
+  }
 
   OpDesc blank(int type) const {
     OpDesc o;
@@ -387,14 +404,14 @@ struct ListBuilder {
 
   void geom(OpDesc& o) {
     const Layout& L = c->lay;
-    const int M = c->cfg.max_verify;
+    const int M = gm;
     if (window && o.wtype == W_BF16 && o.K % 64 == 0 && o.N % kGemvTcRows == 0 &&
-        L.slot_bytes >= kGemvTcRows * 2 * 64) {
+        slot >= kGemvTcRows * 2 * 64) {
       // tensor-core tiles: kGemvTcRows rows x Kc columns in boxes of 64 columns (128-byte swizzle)
       o.tc = 1;
       o.R = kGemvTcRows;
       o.unit = kGemvTcRows;
-      int kc = (L.slot_bytes / (kGemvTcRows * 2 * 64)) * 64;
+      int kc = (slot / (kGemvTcRows * 2 * 64)) * 64;
       o.Kc = std::min(o.K, kc);
       o.csplit = 0;
       o.kw = 0;
@@ -403,14 +420,14 @@ struct ListBuilder {
       const int C = L.n_ctas, groups = (o.N / kGemvTcRows + C - 1) / C;
       const size_t parts = (size_t)kConsumerWarps * groups * kGemvTcRows * M;
       const size_t staged = (size_t)kMmax * o.K + (o.type == OP_OPROJ || o.type == OP_DOWN ? (size_t)groups * kGemvTcRows * M : 0);
-      if (o.type != OP_LMHEAD && groups < kConsumerWarps && (staged + parts) * 4 <= (size_t)L.act_bytes) {
+      if (o.type != OP_LMHEAD && groups < kConsumerWarps && (staged + parts) * 4 <= (size_t)act) {
         o.csplit = 1;
         o.kw = ((o.K + kConsumerWarps - 1) / kConsumerWarps + 63) / 64 * 64;
       }
       encode_tmap(o);
       return;
     }
-    tile_geometry(o.wtype, o.K, o.pair, L.slot_bytes, M, o.R, o.Kc, o.unit);
+    tile_geometry(o.wtype, o.K, o.pair, slot, M, o.R, o.Kc, o.unit);
     // rows too wide for one slot (or for activations in registers): split the columns across
     // the CTA's warps instead of its rows (bf16 / FP8 matrices without expert slots)
     const int cw = o.wtype == W_BF16 ? 8 : (o.wtype == W_FP8 ? 16 : 32);
@@ -420,8 +437,8 @@ struct ListBuilder {
       const int kw = ((o.K + kConsumerWarps - 1) / kConsumerWarps + cw - 1) / cw * cw;
       const int bpc = o.wtype == W_BF16 ? 2 : 1;
       int r = std::min(kRmax, 32 / M);
-      while (r > o.unit && (size_t)r * kw * bpc > (size_t)L.slot_bytes) r -= o.unit;
-      if ((size_t)r * kw * bpc <= (size_t)L.slot_bytes && kw <= 32 * ni * cw) {
+      while (r > o.unit && (size_t)r * kw * bpc > (size_t)slot) r -= o.unit;
+      if ((size_t)r * kw * bpc <= (size_t)slot && kw <= 32 * ni * cw) {
         o.csplit = 1;
         o.Kc = kw;
         o.R = r / o.unit * o.unit;
@@ -597,15 +614,15 @@ struct ListBuilder {
       dn.wait_ctr = rg.ctr;  // routed (and, earlier in every CTA, shared) expert hidden vectors
       dn.aux_ctr = r.ctr;
       dn.x_out = hs_at(2 * l + 2);
-      dn.stage_all = L.exp_stage_all;
+      dn.stage_all = stage_all;
       geom(dn);
       if (dn.stage_all && dn.Kc == dn.K) {
         // slot split: the CTA's rows of each slot in about two chunks, one chunk per warp item
         const int C = L.n_ctas, units = (H / dn.unit + C - 1) / C;
-        const int nr_max = M == 1 ? 10 : 8;  // the kernel's tile rows for one token / a window
+        const int nr_max = gm == 1 ? 10 : 8;  // the kernel's tile rows for one token / a window
         int R = (units + 1) / 2 * dn.unit;
         const size_t row_b = (size_t)I / 2 + I / 32;
-        while (R > dn.unit && (R > nr_max || (size_t)R * row_b + 16 > (size_t)L.slot_bytes)) R -= dn.unit;
+        while (R > dn.unit && (R > nr_max || (size_t)R * row_b + 16 > (size_t)slot)) R -= dn.unit;
         dn.R = R;
         dn.csplit = 1;
       }
@@ -637,8 +654,9 @@ struct ListBuilder {
   }
 };
 
-// Kernel parameters of an op list of n_ops ops at byte offset ops_off of the workspace.
-void fill_params(dec_ctx* c, KParams& k, size_t ops_off, int n_ops) {
+// Kernel parameters of an op list of n_ops ops at byte offset ops_off of the workspace, built
+// with the one-token geometry or the max_verify one.
+void fill_params(dec_ctx* c, KParams& k, size_t ops_off, int n_ops, bool one_token) {
   const dec_config& g = c->cfg;
   const Layout& L = c->lay;
   const int M = g.max_verify, H = g.hidden, C = L.n_ctas;
@@ -666,11 +684,11 @@ void fill_params(dec_ctx* c, KParams& k, size_t ops_off, int n_ops) {
   k.eps = g.rms_eps;
   k.rope_base = g.rope_base;
   k.timeout_ns = g.spin_timeout_ns ? g.spin_timeout_ns : 2000000000ull;
-  k.slot_bytes = L.slot_bytes;
-  k.act_bytes = L.act_bytes;
+  k.slot_bytes = one_token ? L.slot1_bytes : L.slot_bytes;
+  k.act_bytes = one_token ? L.act1_bytes : L.act_bytes;
   k.kv_fp8 = g.kv_dtype == DEC_FP8_E4M3 ? 1 : 0;
   k.xpf_mode = c->xpf_mode;
-  k.attn_tc = c->attn_tc;
+  k.attn_tc = c->attn_tc && k.slot_bytes >= 4 * kAttnTcBoxBytes;  // a tile of keys and values fits a slot
   k.attn_window = g.attn_window;
   k.tmap_k = c->tmap_k;
   k.tmap_v = c->tmap_v;
@@ -694,10 +712,11 @@ void fill_params(dec_ctx* c, KParams& k, size_t ops_off, int n_ops) {
 dec_status build_ops(dec_ctx* c) {
   const dec_config& g = c->cfg;
   c->ops.clear();
-  ListBuilder b(c, c->ops, g.embedding ? X_EMBED : X_HIDDEN_IN);
+  // one-token calls (every call when max_verify is 1): the one-token geometry
+  ListBuilder b(c, c->ops, g.embedding ? X_EMBED : X_HIDDEN_IN, true);
   for (int l = 0; l < g.n_layers; ++l) b.layer(l);
   if (g.vocab) b.head(wsp<float>(c, c->lay.logits));
-  fill_params(c, c->kp, c->lay.ops, (int)c->ops.size());
+  fill_params(c, c->kp, c->lay.ops, (int)c->ops.size(), true);
   // multi-token calls: the same step with the bf16 matrices on tensor-core tiles (one-token
   // calls keep the CUDA-core list above)
   c->wops.clear();
@@ -708,7 +727,7 @@ dec_status build_ops(dec_ctx* c) {
     for (int l = 0; l < g.n_layers; ++l) w.layer(l);
     if (g.vocab) w.head(wsp<float>(c, c->lay.logits));
     if (w.err != DEC_OK) return w.err;
-    fill_params(c, c->wkp, c->lay.wops, (int)c->wops.size());
+    fill_params(c, c->wkp, c->lay.wops, (int)c->wops.size(), false);
   }
   return DEC_OK;
 }
@@ -720,7 +739,7 @@ dec_status ensure_tmaps(dec_ctx* c) {
   const dec_config& g = c->cfg;
   // a tile of keys and values (four boxes) must fit a ring slot: large multi-token staging
   // areas leave smaller slots, and those contexts keep the CUDA-core attention tiles
-  if (!attn_tc_for(&g) || c->lay.slot_bytes < 4 * kAttnTcBoxBytes) {
+  if (!attn_tc_for(&g) || std::max(c->lay.slot_bytes, c->lay.slot1_bytes) < 4 * kAttnTcBoxBytes) {
     c->attn_tc = 0;
     return DEC_OK;
   }
@@ -892,11 +911,12 @@ dec_status run_call(dec_ctx* c, int32_t pos, int m, const int32_t* tokens, const
 // (nullable) receives the list's argmaxes and makes the call wait and check the status word.
 dec_status run_sub(dec_ctx* c, const std::vector<OpDesc>& ops, int32_t pos, int m, const void* hidden,
                    int32_t* argmax_host) {
+  const bool one_token = m == 1;  // the builder chose the geometry the same way
   if ((int)ops.size() > kMaxSubOps) return fail(DEC_ERR_STATE, "%zu ops exceed the sub-list region", ops.size());
   CUDA_TRY(cudaMemcpyAsync(c->ws + c->lay.subops, ops.data(), ops.size() * sizeof(OpDesc), cudaMemcpyHostToDevice,
                            c->stream));
   KParams k;
-  fill_params(c, k, c->lay.subops, (int)ops.size());
+  fill_params(c, k, c->lay.subops, (int)ops.size(), one_token);
   dec_status st = write_state(c, pos, m, nullptr, hidden, 0, nullptr);
   if (st != DEC_OK) return st;
   st = launch_list(c, k, false);
@@ -1105,7 +1125,7 @@ dec_status dec_run_layer(dec_ctx* c, int layer, const void* h_in, int m, int32_t
   st = ensure_tmaps(c);
   if (st != DEC_OK) return st;
   std::vector<OpDesc> ops;
-  ListBuilder b(c, ops, X_HIDDEN_IN);
+  ListBuilder b(c, ops, X_HIDDEN_IN, m == 1);
   b.layer(layer);
   ops.back().y_bf16 = static_cast<uint16_t*>(h_out);  // the layer's last op writes its residual output
   for (OpDesc& o : ops)
@@ -1126,7 +1146,7 @@ dec_status dec_lm_head(dec_ctx* c, const void* h_in, int m, float* logits_dev, i
   dec_status st = check_head(c);
   if (st != DEC_OK) return st;
   std::vector<OpDesc> ops;
-  ListBuilder b(c, ops, X_HIDDEN_IN);
+  ListBuilder b(c, ops, X_HIDDEN_IN, m == 1);
   b.head(logits_dev ? logits_dev : wsp<float>(c, c->lay.logits));
   return run_sub(c, ops, 0, m, h_in, argmax_host);
 }
