@@ -55,5 +55,8 @@ def test_moe_stack_two_layers():
         if top2_margin(inf["logits"]) > 1e-3 * np.max(np.abs(inf["logits"])):
             assert am == inf["token"], (i, am, inf["token"])
         tok = inf["token"]
-    assert checked >= 1, (checked, ambiguous)
+    # seed 0: the oracle leaves 3 of the 4 layer-steps unambiguous (step 1, layer 0 has a relative
+    # 8th/9th gap of 3.6e-4); every one of them must match exactly
+    print(f"top-k checked exactly on {checked} of {checked + ambiguous} layer-steps, {ambiguous} ambiguous")
+    assert checked >= 3, (checked, ambiguous)
     dec.close()
