@@ -23,12 +23,11 @@
 #include <cuda_runtime.h>
 #include <math.h>
 
-#include <mutex>
-
 #include "../../include/dec.h"
 #include "dec_internal.h"
 #include "gemv.cuh"
 #include "ptx.cuh"
+#include "smem_attr.h"
 
 namespace decimpl {
 
@@ -2666,12 +2665,8 @@ __global__ void __launch_bounds__(kThreads, 1) dec_megakernel(const __grid_const
 
 // ------------------------------------------------------------------ host launch
 namespace {
-// Largest dynamic shared-memory size the kernel has been allowed on each device so far: the
-// attribute belongs to the device that was current when it was set, so every device gets its
-// own, and host threads launching at once take the lock.
-constexpr int kMaxDevices = 64;
-std::mutex g_attr_mu;
-size_t g_attr_bytes[kMaxDevices] = {};
+// Largest dynamic shared-memory size the kernel has been allowed on each device so far.
+decimpl::SmemAttrCache g_smem_attr;
 }  // namespace
 
 extern "C" cudaError_t dec_launch_megakernel(const decimpl::KParams* kp, int cooperative, cudaStream_t stream) {
@@ -2680,14 +2675,10 @@ extern "C" cudaError_t dec_launch_megakernel(const decimpl::KParams* kp, int coo
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  {
-    std::lock_guard<std::mutex> lock(g_attr_mu);
-    if (dev < 0 || dev >= kMaxDevices || smem > g_attr_bytes[dev]) {
-      e = cudaFuncSetAttribute(dec_megakernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e != cudaSuccess) return e;
-      if (dev >= 0 && dev < kMaxDevices) g_attr_bytes[dev] = smem;
-    }
-  }
+  e = (cudaError_t)g_smem_attr.ensure(dev, smem, [](size_t bytes) {
+    return (int)cudaFuncSetAttribute(dec_megakernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  });
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)kp->n_ctas);
   cfg.blockDim = dim3(kThreads);
