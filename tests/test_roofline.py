@@ -46,3 +46,20 @@ def test_workload_bytes():
     c3 = synth.moe_layer_shape()
     per_expert = 1536 * (1280 + 80) + 2560 * (384 + 24)
     assert R.algorithmic_bytes(c3, 0) == 2 * 512 * 2560 + 2 * 2560 + 9 * per_expert
+
+
+def test_traffic_figures_follow_their_sources(monkeypatch):
+    """bench.py reports a committed DRAM figure only for the kernel sources it was captured on
+    (their sha256 is stored beside it): same sources, the figure; changed sources, null."""
+    import json
+    import os
+    import bench
+    recs = json.load(open(os.path.join(bench.ROOT, "profiles", "dram_traffic.json")))
+    assert {"dense_2b", "moe_stack", "dense_2b_verify4", "moe_stack_verify4"} <= set(recs)
+    for key, rec in recs.items():
+        assert rec["dram_bytes_per_step"] > 0 and len(rec["source_sha256"]) == 64 and rec["capture"]
+        monkeypatch.setattr(bench, "sources_sha256", lambda files, s=rec["source_sha256"]: s)
+        assert bench.ncu_traffic(key, bench.kernel_sources()) == rec["dram_bytes_per_step"]
+        monkeypatch.setattr(bench, "sources_sha256", lambda files: "0" * 64)
+        assert bench.ncu_traffic(key, bench.kernel_sources()) is None
+    assert bench.ncu_traffic("no_such_workload", bench.kernel_sources()) is None
