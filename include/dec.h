@@ -76,8 +76,8 @@ typedef struct {
   int vocab;         /* V (0: no LM head) */
   int kv_capacity;   /* positions the KV cache holds */
   int max_verify;    /* largest window (tokens per call), 1..4. Above 1 the context keeps a
-                        second op list for multi-token calls (bf16 matrices and attention on
-                        the tensor cores); one-token calls keep a list of their own, as fast
+                        second op list for multi-token calls (bf16 matrices on the tensor
+                        cores); one-token calls keep a list of their own, as fast
                         as in a max_verify = 1 context */
   int embedding;     /* 1: a step starts from E[token]; 0: from a given hidden vector */
   int final_norm;    /* 1: RMSNorm before the LM head */
