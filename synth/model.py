@@ -15,7 +15,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import normal_bf16, tensor_id, start_token
+from . import normal_bf16, tensor_id
 from .configs import ModelShape
 
 
@@ -83,6 +83,3 @@ def hidden_inputs(s: ModelShape, seed: int, m: int) -> np.ndarray:
     """[m, hidden] bf16 ~ N(0,1): the given hidden states of the single-block workloads."""
     return normal_bf16(seed, tensor_id("x_in"), (m, s.hidden))
 
-
-def first_token(s: ModelShape, seed: int) -> int:
-    return start_token(seed, s.vocab)
