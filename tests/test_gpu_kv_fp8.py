@@ -39,7 +39,7 @@ def _compare(shape, seed, steps, **kw):
     sc = _scales(shape, seed)
     cap = shape.kv_prefill + steps + 4
     dec = Decoder(shape, layers, head, experts=experts, kv=kv, capacity=cap, kv_scales=sc, **kw)
-    orc = OracleModel(shape, layers, head, experts=experts, kv=kv, capacity=cap, kv_scales=sc)
+    orc = OracleModel(shape, layers, head, experts=experts, kv=kv, capacity=cap, kv_scales=sc, cache_weights=True)
     # the packer's prefill codes are the oracle's, bit for bit
     for l in range(shape.n_layers):
         n = shape.kv_prefill

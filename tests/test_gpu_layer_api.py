@@ -44,6 +44,7 @@ def test_run_layer_dense_window_and_head(mode):
     for m in (1, 3):
         xs = sm.hidden_inputs(s, seed + m, m)
         orc = oracle_for(s, seed, cap, w=w)  # fresh cache: rows pos.. are the window's own
+        orc.cache_weights = True
         h_out = dec.run_layer(0, _dev(xs), pos)
         got = bf16_to_f64_fast(h_out.cpu().numpy().view(np.uint16))
         refs = []
@@ -81,6 +82,7 @@ def test_run_layer_moe_topk(m):
         pytest.fail("no seed with well-separated router logits")
     dec = decoder_for(s, seed, 8, w=w, max_verify=4)
     orc = oracle_for(s, seed, 8, w=w)
+    orc.cache_weights = True
     h_out, idx, wts = dec.run_layer(0, _dev(xs[:m]), 0, topk=True)
     got = bf16_to_f64_fast(h_out.cpu().numpy().view(np.uint16))
     idx = idx.cpu().numpy()
@@ -103,7 +105,7 @@ def test_lm_head_entry(dtype, m):
     W, targets = plant_margins(sm.head_weights(s, 0)["w_lm"], list(xf), 5, margin=1.0, fp8=(dtype == "fp8"))
     head = {"w_lm": W}
     dec = Decoder(s, [], head, max_verify=m)
-    orc = OracleModel(s, [], head)
+    orc = OracleModel(s, [], head, cache_weights=True)
     am = dec.lm_head(_dev(x))
     lg = dec.logits[:m].cpu().numpy()
     for i in range(m):

@@ -33,7 +33,7 @@ def test_lm_head(built, head_w, dtype, m):
     W, targets = plant_margins(head_w, list(xf), 0, margin=1.0, fp8=(dtype == "fp8"))
     head = {"w_lm": W}
     dec = Decoder(s, [], head, max_verify=m)
-    orc = OracleModel(s, [], head)
+    orc = OracleModel(s, [], head, cache_weights=True)
     xd = torch.from_numpy(x.view(np.int16)).cuda()
     if m == 1:
         am = [dec.step(0, 0, hidden=xd)]

@@ -48,6 +48,7 @@ def moe():
         pytest.fail("no seed with well-separated router logits")
     dec = decoder_for(SHAPE, seed, 8, w=w, max_verify=4)
     orc = oracle_for(SHAPE, seed, 8, w=w)
+    orc.cache_weights = True  # the stored weights, decoded once
     yield seed, xs, dec, orc
     dec.close()
 

@@ -38,7 +38,7 @@ def test_noalloc_lm_head_matches_context(dtype, m, norm):
     W, targets = plant_margins(hw["w_lm"], [f for fs in feats for f in fs], 0, margin=1.0, fp8=(dtype == "fp8"))
     head = {"w_lm": W, **({"final_norm": hw["final_norm"]} if norm else {})}
     dec = Decoder(s, [], head, max_verify=m)
-    orc = OracleModel(s, [], head)
+    orc = OracleModel(s, [], head, cache_weights=True)
     lm = [t for t in dec._tensors if t.kind == B.DEC_T_LM_HEAD][0]
     fn = [t for t in dec._tensors if t.kind == B.DEC_T_FINAL_NORM]
     fn_dev = fn[0].values if norm else None
